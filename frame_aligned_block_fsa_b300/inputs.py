@@ -1,0 +1,77 @@
+"""Seeded synthetic inputs shared by the tests, the benchmark and the oracle checks.
+
+This module only draws random numbers; it holds none of the attention arithmetic.
+
+Recipes (the pages measure on production data, which is not available):
+  normal: Q, K, V i.i.d. N(0, 1), rounded to bf16, layout [H][N][D].
+  stress: every Q and K row is N(0, I_D) times an independent LogNormal(0, 1)
+          scalar (per head, per token); in each head ceil(0.001 N) key tokens,
+          chosen uniformly without replacement, are further scaled by 8;
+          V is N(0, 1).
+All draws come from one CPU torch.Generator seeded with the workload's seed, in
+the order q, k, v (then the stress scalars and outlier choice), so a seed fixes
+the inputs on every machine.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from .workloads import Workload
+
+
+def make_qkv(H: int, N: int, D: int, seed: int, kind: str = "normal"):
+    """Return (q, k, v) as contiguous CPU bf16 tensors of shape [H, N, D]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    q = torch.randn((H, N, D), generator=g, dtype=torch.float32)
+    k = torch.randn((H, N, D), generator=g, dtype=torch.float32)
+    v = torch.randn((H, N, D), generator=g, dtype=torch.float32)
+    if kind == "stress":
+        qs = torch.randn((H, N, 1), generator=g, dtype=torch.float32).exp_()
+        ks = torch.randn((H, N, 1), generator=g, dtype=torch.float32).exp_()
+        q.mul_(qs)
+        k.mul_(ks)
+        n_out = math.ceil(0.001 * N)
+        for h in range(H):
+            idx = torch.randperm(N, generator=g)[:n_out]
+            k[h, idx, :] *= 8.0
+    elif kind != "normal":
+        raise ValueError(f"unknown input kind {kind!r}")
+    return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
+            v.to(torch.bfloat16).contiguous())
+
+
+def make_workload_inputs(wl: Workload):
+    return make_qkv(wl.H, wl.N, wl.D, wl.seed, wl.kind)
+
+
+def sample_rows(wl: Workload, per_head: int, seed: int = 12345):
+    """Stratified row sample: every frame, first/last row of every 16-row group edge
+    that matters (frame starts/ends, 128-row tile edges, the ragged tail of each
+    frame), topped up with uniform random rows.  Returns (heads int32[R], rows int64[R])."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    heads, rows = [], []
+    F, T, N = wl.F, wl.T, wl.N
+    special = set()
+    for f in range(F):
+        base = f * T
+        special.update({base, base + T - 1})
+        for t0 in range(0, T, 128):
+            special.update({base + t0, base + min(t0 + 127, T - 1)})
+    special = sorted(special)
+    for h in range(wl.H):
+        pick = list(special)
+        if len(pick) > per_head:
+            idx = torch.randperm(len(pick), generator=g)[:per_head].tolist()
+            pick = [pick[i] for i in sorted(idx)]
+        extra = per_head - len(pick)
+        if extra > 0:
+            pick += torch.randint(0, N, (extra,), generator=g).tolist()
+        heads += [h] * len(pick)
+        rows += pick
+    import numpy as np
+
+    return np.asarray(heads, dtype=np.int32), np.asarray(rows, dtype=np.int64)

@@ -1,0 +1,40 @@
+"""The five synthetic workloads of frame-structured sparse attention (shapes only).
+
+Tokens are F frames x T tokens per frame; each query frame attends the key frames
+within +-w of itself plus the reference frame `ref`.  The pages give no production
+shapes; these are latent-grid sizes typical of a video super-resolution stage
+(T = 8x8, 16x16, 30x40 and 45x80 latent patches per frame).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    F: int          # frames
+    T: int          # tokens per frame
+    H: int          # heads
+    D: int          # head dim
+    w: int          # window half-width in frames
+    ref: int        # global reference frame
+    block: int      # plan block size: a multiple of 16 dividing T
+    kind: str       # "normal" (i.i.d. N(0,1)) or "stress" (log-normal row norms + outlier keys)
+    seed: int
+
+    @property
+    def N(self) -> int:
+        return self.F * self.T
+
+
+WORKLOADS = {
+    "tiny":   Workload("tiny", F=8, T=64, H=2, D=64, w=1, ref=0, block=16, kind="normal", seed=0),
+    "small":  Workload("small", F=16, T=256, H=8, D=128, w=2, ref=0, block=64, kind="normal", seed=1),
+    "sr28k":  Workload("sr28k", F=24, T=1200, H=24, D=128, w=2, ref=0, block=80, kind="normal", seed=2),
+    "sr57k":  Workload("sr57k", F=16, T=3600, H=16, D=128, w=1, ref=0, block=144, kind="normal", seed=3),
+    "stress": Workload("stress", F=24, T=1200, H=24, D=128, w=4, ref=0, block=80, kind="stress", seed=4),
+}
+
+# The 28.8k-token workload is the one the throughput target is stated on.
+HEADLINE = "sr28k"

@@ -1,0 +1,287 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: hand-derived
+golden fixtures, brute force written independently in Python, closed forms,
+library routines (numpy / scipy) and invariants of softmax attention.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from frame_aligned_block_fsa_b300.inputs import make_qkv
+from frame_aligned_block_fsa_b300.workloads import WORKLOADS
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _read_golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            key, *rest = line.split()
+            vals[key] = [float(x) for x in rest]
+    return vals
+
+
+def _bf16(a):
+    return torch.tensor(np.asarray(a, dtype=np.float32)).to(torch.bfloat16)
+
+
+def _f64(t):
+    return t.to(torch.float64).numpy()
+
+
+# --------------------------------------------------------------------------- plan
+@pytest.mark.parametrize("name", sorted(f for f in os.listdir(GOLDEN) if f.startswith("plan_")))
+def test_plan_matches_hand_derived_golden(oracle_mod, name):
+    g = _read_golden(name)
+    F, T, w, ref, B = (int(g[k][0]) for k in ("F", "T", "w", "ref", "block"))
+    row_ptr, col_idx = oracle_mod.plan(F, T, w, ref, B)
+    assert row_ptr.tolist() == [int(x) for x in g["row_ptr"]]
+    assert col_idx.tolist() == [int(x) for x in g["col_idx"]]
+
+
+# Hand-counted frame pairs (sum over query frames of |S(f)|) for the five workloads:
+#   tiny   F=8,  w=1: 2+3+4*5+3                      = 28
+#   small  F=16, w=2: 3+4+5 + 6*11 + 5+4             = 87
+#   sr28k  F=24, w=2: 3+4+5 + 6*19 + 5+4             = 135
+#   sr57k  F=16, w=1: 2+3 + 4*13 + 3                 = 60
+#   stress F=24, w=4: 5+6+7+8+9 + 10*15 + 9+8+7+6    = 215
+HAND_PAIRS = {"tiny": 28, "small": 87, "sr28k": 135, "sr57k": 60, "stress": 215}
+
+
+@pytest.mark.parametrize("name", list(HAND_PAIRS))
+def test_frame_pairs_and_nnz_closed_form(oracle_mod, name):
+    wl = WORKLOADS[name]
+    assert oracle_mod.active_frame_pairs(wl.F, wl.w, wl.ref) == HAND_PAIRS[name]
+    row_ptr, col_idx = oracle_mod.plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
+    per_frame = wl.T // wl.block
+    assert len(col_idx) == HAND_PAIRS[name] * per_frame * per_frame
+    assert row_ptr[-1] == len(col_idx)
+    # within every row the key blocks ascend strictly
+    for r in range(len(row_ptr) - 1):
+        seg = col_idx[row_ptr[r]:row_ptr[r + 1]]
+        assert np.all(np.diff(seg) > 0)
+
+
+def test_plan_rejects_partial_blocks(oracle_mod):
+    # T=24 with block 16: blocks straddle frame boundaries -> partial blocks exist.
+    with pytest.raises(ValueError):
+        oracle_mod.plan(4, 24, 1, 0, 16)
+
+
+def test_plan_brute_force_small(oracle_mod):
+    # independent restatement: a block pair is active iff its first token pair is allowed
+    for (F, T, w, ref, B) in [(6, 32, 1, 3, 16), (7, 48, 2, 6, 16), (5, 96, 0, 0, 48), (9, 16, 3, 4, 16)]:
+        row_ptr, col_idx = oracle_mod.plan(F, T, w, ref, B)
+        nb = F * T // B
+        expect_ptr, expect_idx = [0], []
+        for qb in range(nb):
+            fq = qb * B // T
+            for kb in range(nb):
+                fk = kb * B // T
+                if abs(fq - fk) <= w or fk == ref:
+                    expect_idx.append(kb)
+            expect_ptr.append(len(expect_idx))
+        assert row_ptr.tolist() == expect_ptr
+        assert col_idx.tolist() == expect_idx
+
+
+# ---------------------------------------------------------------------- attention
+def test_attention_matches_hand_worked_example(oracle_mod):
+    g = _read_golden("attention_F2_T1_D1.txt")
+    q = _bf16(g["q"]).reshape(1, 2, 1)
+    k = _bf16(g["k"]).reshape(1, 2, 1)
+    v = _bf16(g["v"]).reshape(1, 2, 1)
+    res = oracle_mod.attention_full(q, k, v, F=2, T=1, w=0, ref=0, scale=1.0)
+    np.testing.assert_allclose(res["out"][0, :, 0], g["out"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(res["lse"][0], g["lse"], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(res["bound"][0], g["bound"], rtol=0, atol=1e-14)
+
+
+def _brute_force(q, k, v, F, T, w, ref, scale):
+    """Pure-Python restatement: enumerate allowed (i, j) from the frame rule directly."""
+    H, N, D = q.shape
+    out = np.zeros((H, N, D))
+    lse = np.zeros((H, N))
+    for h in range(H):
+        for i in range(N):
+            fi = i // T
+            keys = [j for j in range(N) if abs(fi - j // T) <= w or j // T == ref]
+            logits = [scale * sum(q[h, i, d] * k[h, j, d] for d in range(D)) for j in keys]
+            m = max(logits)
+            e = [math.exp(s - m) for s in logits]
+            l = math.fsum(e)
+            for d in range(D):
+                out[h, i, d] = math.fsum(e[t] * v[h, j, d] for t, j in enumerate(keys)) / l
+            lse[h, i] = m + math.log(l)
+    return out, lse
+
+
+@pytest.mark.parametrize("case", [
+    (2, 3, 4, 1, 8, 1, 0), (1, 4, 3, 0, 4, 1, 2), (2, 3, 5, 2, 8, 7, 1), (1, 2, 8, 0, 16, 0, 1),
+])
+def test_attention_matches_brute_force_tiny(oracle_mod, case):
+    H, F, T, w, D, seed, ref = case
+    q, k, v = make_qkv(H, F * T, D, seed)
+    ref_out, ref_lse = _brute_force(_f64(q), _f64(k), _f64(v), F, T, w, ref, 1 / math.sqrt(D))
+    res = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    np.testing.assert_allclose(res["out"], ref_out, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(res["lse"], ref_lse, rtol=1e-12, atol=1e-13)
+
+
+def test_dense_window_is_textbook_attention(oracle_mod):
+    from scipy.special import logsumexp, softmax
+
+    H, F, T, D = 2, 4, 16, 16
+    q, k, v = make_qkv(H, F * T, D, seed=5)
+    for w in (F - 1, F + 3):
+        res = oracle_mod.attention_full(q, k, v, F, T, w, ref=1)
+        qq, kk, vv = _f64(q), _f64(k), _f64(v)
+        logits = np.einsum("hnd,hmd->hnm", qq, kk) / math.sqrt(D)
+        expect = np.einsum("hnm,hmd->hnd", softmax(logits, axis=-1), vv)
+        np.testing.assert_allclose(res["out"], expect, rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(res["lse"], logsumexp(logits, axis=-1), rtol=1e-12, atol=1e-12)
+
+
+def _allowed_count(F, T, w, ref, f):
+    return T * sum(1 for g in range(F) if abs(f - g) <= w or g == ref)
+
+
+def test_zero_query_gives_mean_of_attended_values(oracle_mod):
+    H, F, T, D, w, ref = 1, 5, 8, 16, 1, 3
+    _, k, v = make_qkv(H, F * T, D, seed=7)
+    q = torch.zeros_like(k)
+    res = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    vv = _f64(v)[0]
+    for i in range(F * T):
+        f = i // T
+        sel = [j for j in range(F * T) if abs(f - j // T) <= w or j // T == ref]
+        np.testing.assert_allclose(res["out"][0, i], vv[sel].mean(axis=0), rtol=1e-13, atol=1e-14)
+        assert res["lse"][0, i] == pytest.approx(math.log(_allowed_count(F, T, w, ref, f)), abs=1e-13)
+
+
+def test_constant_values_give_constant_output(oracle_mod):
+    H, F, T, D = 2, 4, 8, 16
+    q, k, _ = make_qkv(H, F * T, D, seed=8)
+    v = torch.full((H, F * T, D), -1.75, dtype=torch.bfloat16)
+    res = oracle_mod.attention_full(q, k, v, F, T, 1, 0)
+    np.testing.assert_allclose(res["out"], -1.75, rtol=0, atol=1e-14)
+
+
+def test_identical_keys_give_uniform_weights(oracle_mod):
+    H, F, T, D, w, ref = 1, 6, 4, 8, 1, 5
+    q, _, v = make_qkv(H, F * T, D, seed=9)
+    krow = make_qkv(1, 1, D, seed=10)[1][0, 0]
+    k = krow.expand(H, F * T, D).contiguous()
+    res = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    qq, kk, vv = _f64(q)[0], _f64(k)[0], _f64(v)[0]
+    for i in range(F * T):
+        f = i // T
+        sel = [j for j in range(F * T) if abs(f - j // T) <= w or j // T == ref]
+        s = float(qq[i] @ kk[0]) / math.sqrt(D)
+        np.testing.assert_allclose(res["out"][0, i], vv[sel].mean(axis=0), rtol=1e-12, atol=1e-13)
+        assert res["lse"][0, i] == pytest.approx(s + math.log(len(sel)), rel=1e-13, abs=1e-13)
+
+
+def test_weights_sum_to_one_and_vanish_off_mask(oracle_mod):
+    # V rows are the basis vectors e_j, so out_i is the weight row p_i itself.
+    F, T, w, ref = 4, 3, 1, 3
+    N = F * T
+    D = 16
+    q, k, _ = make_qkv(1, N, D, seed=11)
+    v = torch.zeros((1, N, D), dtype=torch.bfloat16)
+    for j in range(N):
+        v[0, j, j] = 1.0
+    res = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    p = res["out"][0]
+    for i in range(N):
+        assert math.fsum(p[i]) == pytest.approx(1.0, abs=1e-12)
+        for j in range(N):
+            allowed = abs(i // T - j // T) <= w or j // T == ref
+            if allowed:
+                assert p[i, j] > 0.0
+            else:
+                assert p[i, j] == 0.0
+        assert np.all(p[i, N:] == 0.0)
+
+
+@pytest.mark.parametrize("kind", ["normal", "stress"])
+def test_bound_form_equals_max_form_and_dominates(oracle_mod, kind):
+    H, F, T, D, w, ref = 2, 6, 16, 32, 1, 0
+    q, k, v = make_qkv(H, F * T, D, seed=13, kind=kind)
+    res = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    ok = ~res["underflow"]
+    assert ok.any()
+    # Cauchy-Schwarz: the row's own bound is never below its true max
+    assert np.all(res["bound"] >= res["rowmax"] - 1e-12 * np.abs(res["bound"]))
+    # exact-arithmetic equality of the two softmax forms on rows that do not underflow
+    np.testing.assert_allclose(res["out_bound"][ok], res["out"][ok], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(res["lse_bound"][ok], res["lse"][ok], rtol=1e-12, atol=1e-12)
+
+
+def test_bound_is_tight_for_parallel_key(oracle_mod):
+    # a key equal to the query and of the largest norm attains the bound exactly
+    D = 4
+    q = _bf16([[1, 2, -2, 4], [0.5, 0.5, 0.5, 0.5]]).reshape(1, 2, D)
+    k = _bf16([[1, 2, -2, 4], [0, 1, 0, 1]]).reshape(1, 2, D)
+    v = _bf16([[1, 0, 0, 0], [0, 1, 0, 0]]).reshape(1, 2, D)
+    res = oracle_mod.attention_full(q, k, v, F=1, T=2, w=0, ref=0)
+    assert res["gap"][0, 0] == pytest.approx(0.0, abs=1e-12)
+    assert res["bound"][0, 0] == pytest.approx(25.0 / 2.0, abs=1e-12)  # |q|^2 / sqrt(4)
+
+
+def test_underflow_flag_and_nan_bound_form(oracle_mod):
+    # D=1, scale 1, T=1 (one token per frame), w=0, reference frame 1.
+    #   frame 0 -> keys {0, 1}: s = -81, -36; m = -36; bound = 9*9 = 81;  gap = 117
+    #   frame 1 -> keys {1}:    s = -36;      m = -36; bound = 9*4 = 36;  gap = 72
+    #   frame 2 -> keys {1, 2}: s = -36, 18;  m = 18;  bound = 9*4 = 36;  gap = 18
+    #   frame 3 -> keys {1, 3}: s = -120, -900; m = -120; bound = 900;  gap = 1020
+    # fp32 underflow iff gap >= 126 ln 2 = 87.34; fp64 itself underflows only past ~745,
+    # where the bound form of the oracle turns into 0/0.
+    q = _bf16([9, 9, 9, 30]).reshape(1, 4, 1)
+    k = _bf16([-9, -4, 2, -30]).reshape(1, 4, 1)
+    v = _bf16([1, 2, 3, 4]).reshape(1, 4, 1)
+    res = oracle_mod.attention_full(q, k, v, F=4, T=1, w=0, ref=1, scale=1.0)
+    np.testing.assert_allclose(res["gap"][0], [117.0, 72.0, 18.0, 1020.0], atol=1e-12)
+    assert res["underflow"][0].tolist() == [True, False, False, True]
+    assert res["out"][0, 0, 0] == pytest.approx(2.0, abs=1e-12)
+    assert res["out_bound"][0, 0, 0] == pytest.approx(2.0, abs=1e-12)
+    assert res["out"][0, 3, 0] == pytest.approx(2.0, abs=1e-12)
+    assert math.isnan(res["out_bound"][0, 3, 0])
+    assert res["out"][0, 2, 0] == pytest.approx((3 + 2 * math.exp(-54)) / (1 + math.exp(-54)), abs=1e-14)
+
+
+# -------------------------------------------------------------------------- norms
+@pytest.mark.parametrize("kind", ["normal", "stress"])
+def test_norms_against_library_routines_and_gap_bound(oracle_mod, kind):
+    H, F, T, D, w, ref = 2, 5, 16, 32, 1, 2
+    q, k, v = make_qkv(H, F * T, D, seed=21, kind=kind)
+    nm = oracle_mod.norms(q, k, F, T, w, ref)
+    qq, kk = _f64(q), _f64(k)
+    np.testing.assert_allclose(nm["qnorm"], np.linalg.norm(qq, axis=-1), rtol=1e-14)
+    kn = np.linalg.norm(kk, axis=-1).reshape(H, F, T)
+    np.testing.assert_allclose(nm["kmax"], kn.max(axis=-1), rtol=1e-14)
+    att = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    # the per-frame-max route and the per-row-key-set route give the same bound
+    np.testing.assert_allclose(nm["bound"], att["bound"], rtol=1e-13)
+    # the eligibility statistic bounds the true gap from above
+    assert np.all(nm["gap_hat"] >= att["gap"] - 1e-9)
+    # eligibility is the threshold test on the per-head worst gap bound
+    for tau in (0.5, 5.0, 50.0, 1e6):
+        e = oracle_mod.norms(q, k, F, T, w, ref, tau=tau)["eligible"]
+        assert e.tolist() == [int(x <= tau) for x in nm["gap_hat"].max(axis=1)]
+
+
+def test_active_flops_formula_matches_enumeration(oracle_mod):
+    wl = WORKLOADS["small"]
+    row_ptr, col_idx = oracle_mod.plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
+    # every active block pair contributes QK^T and PV: 2 * (2 * B * B * D) flops per head
+    expect = len(col_idx) * 4 * wl.block * wl.block * wl.D * wl.H
+    assert oracle_mod.active_flops(wl.F, wl.T, wl.w, wl.ref, wl.H, wl.D) == expect
