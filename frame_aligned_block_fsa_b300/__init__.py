@@ -1,1 +1,17 @@
-"""Frame-aligned block-sparse attention with a norm-bound softmax, for B300 (sm_103a)."""
+"""Frame-aligned block-sparse attention with a norm-bound softmax, for B300 (sm_103a).
+
+Public API (thin wrappers over the C ABI in include/fsa.h; every step runs in libfsa.so):
+
+    plan = Plan(F, T, w, ref, block)           # fsa_plan
+    norms(q, k, plan, qnorm, kmax, bound, eligible)   # fsa_norms
+    out, lse = forward(q, k, v, plan, mode)    # fsa_forward, mode "norm_bound" | "online_max"
+    forward_ex(...)                            # fsa_forward_ex
+
+The library is loaded lazily on first use; importing the package needs no GPU.
+"""
+from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_TIMEOUT, FSA_ERR_UNSUPPORTED, FSA_OK,  # noqa: F401
+                   FsaError, Plan, forward, forward_ex, load, new_stats, norms, read_stats,
+                   selftest_wait_timeout, status_string)
+
+__all__ = ["Plan", "norms", "forward", "forward_ex", "new_stats", "read_stats", "selftest_wait_timeout",
+           "status_string", "load", "FsaError"]

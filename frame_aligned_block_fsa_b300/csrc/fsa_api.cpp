@@ -1,0 +1,452 @@
+// fsa_api.cpp -- the C ABI: argument checks, the frame-aligned block plan, device data,
+// tensor maps and kernel launches.  See include/fsa.h for the contract of every call.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "fsa.h"
+#include "fsa_internal.h"
+
+using fsa::kMaxRuns;
+using fsa::kRunStride;
+
+struct fsa_plan_s {
+    int F = 0, T = 0, w = 0, ref = 0, block = 0;
+    int64_t N = 0;
+    std::vector<int32_t> row_ptr, col_idx;  // block CSR
+    std::vector<int32_t> runs;              // [F][kRunStride], tokens within a head
+    std::vector<int32_t> items;             // [n_items][4]
+    int n_items = 0;
+    float tau = 64.0f;
+    int key_tile = 0;                       // 0 = automatic
+    std::mutex mu;
+    // device data, created on first device use
+    int device = -1;
+    int32_t* d_runs = nullptr;
+    int32_t* d_items = nullptr;
+    // norms workspace, grown on demand (capacities in elements)
+    int64_t cap_qnorm = 0, cap_bound = 0, cap_kmax = 0, cap_ksum = 0, cap_gmax = 0, cap_elig = 0;
+    float* d_qnorm = nullptr;
+    float* d_bound = nullptr;
+    float* d_kmax = nullptr;
+    float* d_ksum = nullptr;
+    unsigned* d_gmax = nullptr;
+    uint8_t* d_elig = nullptr;
+};
+
+namespace {
+
+constexpr long long kDefaultWaitLimit = 4000000000LL;  // SM clock cycles (about 2 s)
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? FSA_OK : FSA_ERR_CUDA; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Largest multiple of 16 that divides T and is at most 128.
+int auto_key_tile(int T)
+{
+    for (int nk = 128; nk >= 16; nk -= 16)
+        if (T % nk == 0) return nk;
+    return 0;
+}
+
+int check_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FSA_ERR_UNSUPPORTED;  // built for sm_103a only
+    return FSA_OK;
+}
+
+template <typename T>
+int upload(T** dst, const std::vector<T>& src)
+{
+    if (cudaMalloc(reinterpret_cast<void**>(dst), std::max<size_t>(1, src.size()) * sizeof(T)) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    if (!src.empty() && cudaMemcpy(*dst, src.data(), src.size() * sizeof(T), cudaMemcpyHostToDevice) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    return FSA_OK;
+}
+
+// First device use: check the device and upload the key runs and the work list.
+int ensure_device(fsa_plan_s* P)
+{
+    int rc = check_device();
+    if (rc != FSA_OK) return rc;
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (P->device == dev) return FSA_OK;
+    if (P->device != -1) return FSA_ERR_INVALID_ARG;  // a plan serves one device
+    if ((rc = upload(&P->d_runs, P->runs)) != FSA_OK) return rc;
+    if ((rc = upload(&P->d_items, P->items)) != FSA_OK) return rc;
+    P->device = dev;
+    return FSA_OK;
+}
+
+template <typename T>
+int grow(T** p, int64_t* cap, int64_t need)
+{
+    if (*cap >= need) return FSA_OK;
+    if (*p) cudaFree(*p);
+    *p = nullptr;
+    *cap = 0;
+    if (cudaMalloc(reinterpret_cast<void**>(p), static_cast<size_t>(need) * sizeof(T)) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    *cap = need;
+    return FSA_OK;
+}
+
+int ensure_workspace(fsa_plan_s* P, int H, int D)
+{
+    const int64_t hn = static_cast<int64_t>(H) * P->N;
+    const int64_t hf = static_cast<int64_t>(H) * P->F;
+    int rc;
+    if ((rc = grow(&P->d_qnorm, &P->cap_qnorm, hn)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_bound, &P->cap_bound, hn)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_kmax, &P->cap_kmax, hf)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_ksum, &P->cap_ksum, hf * D)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_gmax, &P->cap_gmax, static_cast<int64_t>(H))) != FSA_OK) return rc;
+    return grow(&P->d_elig, &P->cap_elig, static_cast<int64_t>(H));
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// bf16 [rows][D] row-major, boxes of 64 columns (128 bytes, the swizzle span) x box_rows.
+int make_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int D, int box_rows)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc) return FSA_ERR_CUDA;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+    cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FSA_OK : FSA_ERR_CUDA;
+}
+
+int check_shape(const fsa_plan_s* P, int H, int D)
+{
+    if (!P || H < 0) return FSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(H) * P->N >= (int64_t(1) << 31)) return FSA_ERR_INVALID_ARG;
+    return FSA_OK;
+}
+
+int run_norms(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, int H, int D, float* qnorm, float* kmax,
+              float* bound, uint8_t* eligible, cudaStream_t stream)
+{
+    fsa::NormsLaunch L;
+    L.q = q;
+    L.k = k;
+    L.H = H;
+    L.D = D;
+    L.F = P->F;
+    L.T = P->T;
+    L.N = static_cast<int>(P->N);
+    L.runs = P->d_runs;
+    L.scale = 1.0f / std::sqrt(static_cast<float>(D));
+    L.tau = P->tau;
+    L.qnorm = qnorm;
+    L.kmax = kmax ? kmax : P->d_kmax;
+    L.ksum = P->d_ksum;
+    L.bound = bound ? bound : P->d_bound;
+    L.gmax = P->d_gmax;
+    L.eligible = eligible ? eligible : P->d_elig;
+    L.stream = stream;
+    const int rc = fsa::launch_norms(L);
+    return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fsa_status_string(int status)
+{
+    switch (status) {
+        case FSA_OK: return "ok";
+        case FSA_ERR_INVALID_ARG: return "invalid argument";
+        case FSA_ERR_UNSUPPORTED: return "unsupported";
+        case FSA_ERR_CUDA: return "cuda error";
+        case FSA_ERR_TIMEOUT: return "device wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int fsa_plan(int F, int T, int w, int ref, int block, fsa_plan_t* out)
+{
+    if (!out) return FSA_ERR_INVALID_ARG;
+    if (F < 1 || T < 16 || w < 0 || ref < 0 || ref >= F) return FSA_ERR_INVALID_ARG;
+    if (block < 16 || block % 16 != 0 || T % block != 0) return FSA_ERR_INVALID_ARG;
+    const int64_t N = static_cast<int64_t>(F) * T;
+    if (N >= (int64_t(1) << 31)) return FSA_ERR_INVALID_ARG;
+    fsa_plan_s* P = new (std::nothrow) fsa_plan_s();
+    if (!P) return FSA_ERR_INVALID_ARG;
+    P->F = F;
+    P->T = T;
+    P->w = w;
+    P->ref = ref;
+    P->block = block;
+    P->N = N;
+
+    // Key frames of every query frame: the window [f-w, f+w] clipped to [0, F) plus the
+    // reference frame, each counted once, ascending.
+    auto key_frames = [&](int f) {
+        std::vector<int> g;
+        for (int x = 0; x < F; ++x)
+            if (std::abs(f - x) <= w || x == ref) g.push_back(x);
+        return g;
+    };
+
+    // Block CSR: blocks never straddle a frame because block divides T.
+    const int bpf = T / block;  // blocks per frame
+    const int64_t nb = N / block;
+    int64_t nnz = 0;
+    for (int f = 0; f < F; ++f) nnz += static_cast<int64_t>(key_frames(f).size()) * bpf * bpf;
+    if (nnz >= (int64_t(1) << 31)) {
+        delete P;
+        return FSA_ERR_INVALID_ARG;
+    }
+    try {
+        P->row_ptr.resize(static_cast<size_t>(nb + 1));
+        P->col_idx.reserve(static_cast<size_t>(nnz));
+        P->row_ptr[0] = 0;
+        for (int64_t qb = 0; qb < nb; ++qb) {
+            const int f = static_cast<int>(qb / bpf);
+            for (int g : key_frames(f))
+                for (int b = 0; b < bpf; ++b) P->col_idx.push_back(g * bpf + b);
+            P->row_ptr[qb + 1] = static_cast<int32_t>(P->col_idx.size());
+        }
+
+        // Key runs per query frame, read off the CSR row of the frame's first block:
+        // consecutive key blocks merge into one contiguous run of tokens.
+        P->runs.assign(static_cast<size_t>(F) * kRunStride, 0);
+        for (int f = 0; f < F; ++f) {
+            const int64_t qb = static_cast<int64_t>(f) * bpf;
+            int32_t* R = &P->runs[static_cast<size_t>(f) * kRunStride];
+            int n = 0;
+            int64_t prev = -2;
+            for (int32_t e = P->row_ptr[qb]; e < P->row_ptr[qb + 1]; ++e) {
+                const int64_t kb = P->col_idx[e];
+                if (kb == prev + 1) {
+                    R[2 * n] += block;  // extend the current run
+                } else {
+                    if (n == kMaxRuns) {
+                        delete P;
+                        return FSA_ERR_UNSUPPORTED;
+                    }
+                    R[1 + 2 * n] = static_cast<int32_t>(kb * block);
+                    R[2 + 2 * n] = block;
+                    ++n;
+                }
+                prev = kb;
+            }
+            R[0] = n;
+        }
+
+        // Work items: pairs of 128-row query tiles inside one frame (the last tile of a frame
+        // may be ragged, a frame with an odd tile count ends with a single tile).  Longest
+        // first; the kernel adds the head index on top (head-major launch order).
+        const int n_qt = (T + 127) / 128;
+        const int n_pairs = (n_qt + 1) / 2;
+        struct Item {
+            int64_t cost;
+            int f, pair;
+        };
+        std::vector<Item> order;
+        for (int f = 0; f < F; ++f) {
+            int64_t keys = 0;
+            const int32_t* R = &P->runs[static_cast<size_t>(f) * kRunStride];
+            for (int r = 0; r < R[0]; ++r) keys += R[2 + 2 * r];
+            for (int pr = 0; pr < n_pairs; ++pr) {
+                const int rows = std::min(256, T - 256 * pr);
+                order.push_back({keys * (rows > 128 ? 2 : 1), f, pr});
+            }
+        }
+        std::stable_sort(order.begin(), order.end(), [](const Item& a, const Item& b) { return a.cost > b.cost; });
+        P->n_items = static_cast<int>(order.size());
+        P->items.resize(order.size() * 4);
+        for (size_t i = 0; i < order.size(); ++i) {
+            const int r0 = 256 * order[i].pair;
+            P->items[4 * i + 0] = order[i].f;
+            P->items[4 * i + 1] = order[i].f * T + r0;
+            P->items[4 * i + 2] = std::min(128, T - r0);
+            P->items[4 * i + 3] = std::max(0, std::min(128, T - r0 - 128));
+        }
+    } catch (...) {
+        delete P;
+        return FSA_ERR_INVALID_ARG;
+    }
+    *out = P;
+    return FSA_OK;
+}
+
+void fsa_plan_destroy(fsa_plan_t plan)
+{
+    if (!plan) return;
+    if (plan->device != -1) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        cudaSetDevice(plan->device);
+        cudaDeviceSynchronize();
+        cudaFree(plan->d_runs);
+        cudaFree(plan->d_items);
+        cudaFree(plan->d_qnorm);
+        cudaFree(plan->d_bound);
+        cudaFree(plan->d_kmax);
+        cudaFree(plan->d_ksum);
+        cudaFree(plan->d_gmax);
+        cudaFree(plan->d_elig);
+        if (cur >= 0) cudaSetDevice(cur);
+    }
+    delete plan;
+}
+
+int fsa_plan_export(fsa_plan_t plan, int32_t* row_ptr, int32_t* col_idx, int64_t* nnz)
+{
+    if (!plan) return FSA_ERR_INVALID_ARG;
+    if (nnz) *nnz = static_cast<int64_t>(plan->col_idx.size());
+    if (row_ptr) std::memcpy(row_ptr, plan->row_ptr.data(), plan->row_ptr.size() * sizeof(int32_t));
+    if (col_idx && !plan->col_idx.empty())
+        std::memcpy(col_idx, plan->col_idx.data(), plan->col_idx.size() * sizeof(int32_t));
+    return FSA_OK;
+}
+
+int fsa_plan_set_tau(fsa_plan_t plan, float tau)
+{
+    if (!plan || !(tau > 0.0f)) return FSA_ERR_INVALID_ARG;
+    plan->tau = tau;
+    return FSA_OK;
+}
+
+int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile)
+{
+    if (!plan) return FSA_ERR_INVALID_ARG;
+    if (key_tile != 0 && (key_tile < 16 || key_tile > 128 || key_tile % 16 != 0 || plan->T % key_tile != 0))
+        return FSA_ERR_INVALID_ARG;
+    plan->key_tile = key_tile;
+    return FSA_OK;
+}
+
+int fsa_norms(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t plan, float* qnorm, float* kmax,
+              float* bound, uint8_t* eligible, void* stream)
+{
+    int rc = check_shape(plan, H, D);
+    if (rc != FSA_OK) return rc;
+    if (H == 0) return FSA_OK;
+    if (!q || !k || !aligned16(q) || !aligned16(k)) return FSA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if ((rc = ensure_device(plan)) != FSA_OK) return rc;
+    if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
+    return run_norms(plan, q, k, H, D, qnorm, kmax, bound, eligible, static_cast<cudaStream_t>(stream));
+}
+
+int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,
+                   fsa_plan_t plan, int mode, const float* bound, const uint8_t* eligible, float* rowmax,
+                   fsa_stats_t* dev_stats, void* stream)
+{
+    int rc = check_shape(plan, H, D);
+    if (rc != FSA_OK) return rc;
+    if (mode != FSA_MODE_NORM_BOUND && mode != FSA_MODE_ONLINE_MAX) return FSA_ERR_INVALID_ARG;
+    if ((bound == nullptr) != (eligible == nullptr)) return FSA_ERR_INVALID_ARG;
+    if (H == 0) return FSA_OK;  // empty problem: nothing to read or write
+    if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FSA_ERR_INVALID_ARG;
+    const int NK = plan->key_tile ? plan->key_tile : auto_key_tile(plan->T);
+    if (NK == 0) return FSA_ERR_UNSUPPORTED;
+    for (int f = 0; f < plan->F; ++f) {
+        const int32_t* R = &plan->runs[static_cast<size_t>(f) * kRunStride];
+        for (int r = 0; r < R[0]; ++r)
+            if (R[2 + 2 * r] % NK != 0) return FSA_ERR_UNSUPPORTED;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if ((rc = ensure_device(plan)) != FSA_OK) return rc;
+    if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
+    if (mode == FSA_MODE_NORM_BOUND && bound == nullptr) {
+        if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
+        if ((rc = run_norms(plan, q, k, H, D, nullptr, nullptr, nullptr, nullptr, st)) != FSA_OK) return rc;
+        bound = plan->d_bound;
+        eligible = plan->d_elig;
+    }
+    const int64_t rows = static_cast<int64_t>(H) * plan->N;
+    CUtensorMap mq, mk, mv;
+    if ((rc = make_tensor_map(&mq, q, rows, D, 128)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mk, k, rows, D, NK)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
+    fsa::AttnLaunch L;
+    L.D = D;
+    L.NK = NK;
+    L.H = H;
+    L.tmQ = &mq;
+    L.tmK = &mk;
+    L.tmV = &mv;
+    L.stream = st;
+    L.params.items = plan->d_items;
+    L.params.runs = plan->d_runs;
+    L.params.n_items = plan->n_items;
+    L.params.N = static_cast<int>(plan->N);
+    L.params.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    L.params.mode = mode;
+    L.params.bound = bound;
+    L.params.eligible = eligible;
+    L.params.out = out;
+    L.params.lse = lse;
+    L.params.rowmax = rowmax;
+    L.params.stats = dev_stats;
+    L.params.wait_limit = kDefaultWaitLimit;
+    rc = fsa::launch_attention(L);
+    return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}
+
+int fsa_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,
+                fsa_plan_t plan, int mode, void* stream)
+{
+    return fsa_forward_ex(q, k, v, out, lse, H, D, plan, mode, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+int fsa_selftest_wait_timeout(long long limit_cycles, int32_t* status, void* stream)
+{
+    if (!status || limit_cycles <= 0) return FSA_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc != FSA_OK) return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* d = nullptr;
+    if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) return FSA_ERR_CUDA;
+    rc = cuda_status(cudaMemsetAsync(d, 0, sizeof(int), st));
+    if (rc == FSA_OK && fsa::launch_selftest_wait(limit_cycles, d, st) != 0) rc = FSA_ERR_CUDA;
+    if (rc == FSA_OK) rc = cuda_status(cudaMemcpyAsync(status, d, sizeof(int), cudaMemcpyDeviceToHost, st));
+    if (rc == FSA_OK) rc = cuda_status(cudaStreamSynchronize(st));
+    cudaFree(d);
+    return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,64 @@
+// fsa_internal.h -- structures shared by the host API and the kernels (not part of the ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fsa.h"
+
+namespace fsa {
+
+// Key runs of one query frame: [n_runs, start_0, len_0, start_1, len_1, ...] in tokens of a
+// head; every run is a union of whole frames, ascending, disjoint.
+constexpr int kMaxRuns = 4;
+constexpr int kRunStride = 1 + 2 * kMaxRuns;
+
+struct AttnParams {
+    const int32_t* items;  // [n_items][4]: query frame, first query row (token), valid rows tile 0, tile 1
+    const int32_t* runs;   // [F][kRunStride]
+    int n_items;
+    int N;                 // tokens per head
+    float scale_log2;      // c * log2(e)
+    int mode;              // 0 norm_bound, 1 online_max
+    const float* bound;    // [H][N] or null
+    const uint8_t* eligible;  // [H] or null
+    float* out;            // [H][N][D]
+    float* lse;            // [H][N]
+    float* rowmax;         // [H][N] or null
+    fsa_stats_t* stats;    // or null
+    long long wait_limit;  // clock cycles
+};
+
+struct AttnLaunch {
+    int D, NK, H;
+    const CUtensorMap* tmQ;
+    const CUtensorMap* tmK;
+    const CUtensorMap* tmV;
+    AttnParams params;
+    cudaStream_t stream;
+};
+
+int launch_attention(const AttnLaunch& L);
+int attn_smem_bytes(int D, int NK);
+int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);
+
+struct NormsLaunch {
+    const uint16_t* q;
+    const uint16_t* k;
+    int H, D, F, T, N;
+    const int32_t* runs;   // device [F][kRunStride]
+    float scale;
+    float tau;
+    float* qnorm;          // [H][N] or null
+    float* kmax;           // [H][F]
+    float* ksum;           // [H][F][D] workspace
+    float* bound;          // [H][N]
+    unsigned* gmax;        // [H] workspace
+    uint8_t* eligible;     // [H]
+    cudaStream_t stream;
+};
+
+int launch_norms(const NormsLaunch& L);
+
+}  // namespace fsa

@@ -1,0 +1,175 @@
+/*
+ * fsa.h -- frame-aligned block-sparse attention with a norm-bound softmax, for B300 (sm_103a).
+ *
+ * What it computes.  Tokens are F frames x T tokens per frame (N = F*T per head).
+ * A query in frame f attends every key whose frame g satisfies |f - g| <= w, or
+ * g == ref (one global reference frame); the window is clipped at the sequence
+ * ends and the reference frame is counted once.  For every head h and query
+ * row i the library returns
+ *     out[h][i] = softmax_j( c <q_i, k_j> ) v_j   over the attended keys j,
+ *     lse[h][i] = ln sum_j exp( c <q_i, k_j> ),   c = 1/sqrt(D),
+ * which is exactly masked softmax attention over those frame pairs.
+ * Source: "HeyGen toi uu hoa mo hinh Avatar IV tren Google Cloud Trillium TPU"
+ * (aihot.vn), section "Xoa bo mat na" (window + reference frame, block size a
+ * multiple of 16 that divides a frame, Fig. 3) and section "Giai phong Softmax"
+ * (fixed per-row upper bound from precomputed norms instead of a running max,
+ * per-head fallback to the running max inside the same kernel, Fig. 4).
+ *
+ * Layouts (all row-major, contiguous, caller-owned device memory):
+ *   q, k, v   bf16 [H][N][D], passed as 16-bit patterns (uint16_t), 16-byte aligned
+ *   out       fp32 [H][N][D]
+ *   lse       fp32 [H][N]   (natural log)
+ *   qnorm     fp32 [H][N],  kmax fp32 [H][F],  bound fp32 [H][N],  eligible uint8 [H]
+ * D must be 64 or 128.  H*N must stay below 2^31.
+ *
+ * Streams: every device call is asynchronous on the given stream (a cudaStream_t
+ * passed as void*; NULL = legacy default stream).  Nothing synchronises the host
+ * except fsa_plan_destroy and the first device use of a plan (see fsa_plan).
+ *
+ * Errors: every call returns an int status (fsa_status) and never throws.  Invalid
+ * arguments are rejected before any device work is enqueued.
+ */
+#ifndef FSA_H_
+#define FSA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fsa_plan_s* fsa_plan_t; /* opaque, library-owned */
+
+enum fsa_mode {
+    FSA_MODE_NORM_BOUND = 0, /* fixed per-row bound; heads that fail eligibility fall back */
+    FSA_MODE_ONLINE_MAX = 1  /* running max with accumulator rescale on every head */
+};
+
+enum fsa_status {
+    FSA_OK = 0,
+    FSA_ERR_INVALID_ARG = -1, /* bad shape, null pointer, block does not tile the frames */
+    FSA_ERR_UNSUPPORTED = -2, /* D not in {64,128}, device is not sm_103, plan shape not handled */
+    FSA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+    FSA_ERR_TIMEOUT = -4      /* a bounded device-side wait gave up (reported via fsa_stats_t) */
+};
+
+/* Device-side statistics, written by fsa_forward_ex when the caller passes a
+ * device pointer to one of these.  The call zeroes it first (on the stream). */
+typedef struct fsa_stats {
+    int32_t error;          /* 0, or FSA_ERR_TIMEOUT if a bounded wait inside a kernel gave up */
+    int32_t timeout_site;   /* diagnostic: which wait gave up (0 if none) */
+    int32_t fallback_heads; /* heads run with the running max although norm_bound was requested */
+    int32_t reserved0;
+    int64_t underflow_rows; /* rows whose bound gap is >= 126 ln 2 (known only where the row max is
+                               tracked and a bound is available) or whose row sum underflowed */
+    int64_t reserved1;
+} fsa_stats_t;
+
+/*
+ * fsa_plan -- build the frame-aligned active block list (host only, no device work).
+ * Source: aihot.vn page above, section "Xoa bo mat na" and Fig. 3: with a block size
+ * that is a multiple of 16 and divides T, every block pair is fully inside the mask
+ * or fully outside it, so no tile needs a mask predicate or padding.
+ *   F >= 1 frames, T >= 16 tokens per frame, w >= 0 window half-width in frames,
+ *   0 <= ref < F reference frame, block: multiple of 16 dividing T.
+ * The plan holds the block CSR (query blocks ascending, key blocks ascending within a
+ * row) and the per-frame key runs the kernel walks.  *out receives a new plan on
+ * FSA_OK and is untouched otherwise.  Device data (the work list and a workspace for
+ * the norms) is created lazily by the first fsa_norms / fsa_forward* call on the
+ * then-current device, which allocates device memory and therefore should come
+ * before any stream capture.  A plan must not be used from two streams at once.
+ * Errors: FSA_ERR_INVALID_ARG for out == NULL, a bad shape, or F*T >= 2^31.
+ */
+int fsa_plan(int F, int T, int w, int ref, int block, fsa_plan_t* out);
+
+/* Free a plan and its device data (synchronises the device if it holds any). NULL is a no-op. */
+void fsa_plan_destroy(fsa_plan_t plan);
+
+/*
+ * fsa_plan_export -- copy the block CSR to host memory.
+ *   row_ptr: int32 [N/block + 1] or NULL;  col_idx: int32 [nnz] or NULL;  nnz: int64 out or NULL.
+ * Call once with NULL arrays to learn nnz.  Host only.
+ */
+int fsa_plan_export(fsa_plan_t plan, int32_t* row_ptr, int32_t* col_idx, int64_t* nnz);
+
+/*
+ * fsa_plan_set_tau -- eligibility threshold (nats) on the per-head gap bound used by
+ * norm_bound mode.  A head is eligible for the fixed bound iff for all its rows
+ *     c ( ||q_i|| Kmax_S(f) - <q_i, kbar_S(f)> ) <= tau,
+ * an upper bound on (bound - row max) because the max logit is at least the mean
+ * logit.  The pages check eligibility per head but give no criterion or number;
+ * the default is 64 (exp(-64) stays far above the fp32 normal range).  tau > 0.
+ */
+int fsa_plan_set_tau(fsa_plan_t plan, float tau);
+
+/*
+ * fsa_plan_set_key_tile -- key rows per tensor-core tile: 0 = automatic (the largest
+ * multiple of 16 that divides T and is <= 128), else a multiple of 16 in [16, 128]
+ * dividing T.  Results are bitwise independent of `block`; they may change in the
+ * last bits with the key tile (summation order).
+ */
+int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
+
+/*
+ * fsa_norms -- the precomputed norm arrays of the bound.
+ * Source: aihot.vn page above, section "Giai phong Softmax": by Cauchy-Schwarz the
+ * largest logit of a query is at most its norm times the largest key norm; a small
+ * array of precomputed norms lets every row fix its bound when it starts.
+ *   qnorm[h][n]  = ||q_{h,n}||                                (fp32 sum of bf16 squares)
+ *   kmax[h][g]   = max over keys n of frame g of ||k_{h,n}||
+ *   bound[h][n]  = c * qnorm[h][n] * max_{g in S(frame(n))} kmax[h][g]
+ *   eligible[h]  = 1 iff the head passes the tau test of fsa_plan_set_tau
+ * q, k: device bf16 [H][N][D].  Any output pointer may be NULL (the value is then kept
+ * only in the plan's workspace).  Uses plan-owned workspace (per-frame key sums).
+ * Errors: FSA_ERR_INVALID_ARG (q/k NULL, H < 0), FSA_ERR_UNSUPPORTED (D, device),
+ * FSA_ERR_CUDA (launch or allocation failure).  H == 0 is a no-op.
+ */
+int fsa_norms(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t plan,
+              float* qnorm, float* kmax, float* bound, uint8_t* eligible, void* stream);
+
+/*
+ * fsa_forward -- frame-aligned sparse attention, one pass over window + reference frame.
+ * Source: aihot.vn page above, "Xoa bo mat na" (single pass, no masks, no merge) and
+ * "Giai phong Softmax" (norm-bound softmax with per-head in-kernel fallback).
+ *   mode FSA_MODE_NORM_BOUND: runs fsa_norms into the plan's workspace, then the
+ *        attention kernel with p = exp(s - bound_i) (no running max, no rescale) on
+ *        eligible heads and the running max on the others;
+ *   mode FSA_MODE_ONLINE_MAX: the attention kernel with a running max on every head.
+ * q, k, v device bf16 [H][N][D]; out device fp32 [H][N][D]; lse device fp32 [H][N].
+ * Errors as fsa_norms, plus FSA_ERR_INVALID_ARG for a bad mode or NULL tensor.
+ */
+int fsa_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse,
+                int H, int D, fsa_plan_t plan, int mode, void* stream);
+
+/*
+ * fsa_forward_ex -- fsa_forward with caller-supplied norms and optional diagnostics.
+ *   bound, eligible: device arrays as produced by fsa_norms (both or neither).  When
+ *        given, the norms pass is skipped and these are used as they are; when NULL in
+ *        norm_bound mode, fsa_norms runs into the plan's workspace first.
+ *   rowmax: optional device fp32 [H][N]; rows that ran with the running max receive
+ *        their max logit c <q_i, k_j> (natural units), rows that ran with the fixed
+ *        bound receive NaN (they never form the max).
+ *   dev_stats: optional device fsa_stats_t, zeroed by this call, then filled by the
+ *        kernels (timeouts, fallback heads, underflow rows).
+ */
+int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse,
+                   int H, int D, fsa_plan_t plan, int mode,
+                   const float* bound, const uint8_t* eligible, float* rowmax,
+                   fsa_stats_t* dev_stats, void* stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* fsa_status_string(int status);
+
+/*
+ * fsa_selftest_wait_timeout -- checks the bounded-wait path without faulting the GPU.
+ * Launches one tiny kernel whose only thread waits, through the same bounded mbarrier
+ * wait the attention kernel uses, on a barrier nothing arrives at, with a limit of
+ * limit_cycles SM clock cycles.  *status receives the code the kernel reported
+ * (FSA_ERR_TIMEOUT when the wait gave up as designed).  Synchronises the stream.
+ */
+int fsa_selftest_wait_timeout(long long limit_cycles, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* FSA_H_ */
