@@ -51,10 +51,10 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? FSA_OK : FSA_ERR_CUDA
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Largest multiple of 16 that divides T and is at most 128.
-int auto_key_tile(int T)
+// Largest multiple of 16 that divides T and fits the kernel's TMEM budget for this D.
+int auto_key_tile(int T, int D)
 {
-    for (int nk = 128; nk >= 16; nk -= 16)
+    for (int nk = fsa::kMaxKeyTile(D); nk >= 16; nk -= 16)
         if (T % nk == 0) return nk;
     return 0;
 }
@@ -380,8 +380,8 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
     if (H == 0) return FSA_OK;  // empty problem: nothing to read or write
     if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FSA_ERR_INVALID_ARG;
-    const int NK = plan->key_tile ? plan->key_tile : auto_key_tile(plan->T);
-    if (NK == 0) return FSA_ERR_UNSUPPORTED;
+    const int NK = plan->key_tile ? plan->key_tile : auto_key_tile(plan->T, D);
+    if (NK == 0 || NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
     for (int f = 0; f < plan->F; ++f) {
         const int32_t* R = &plan->runs[static_cast<size_t>(f) * kRunStride];
         for (int r = 0; r < R[0]; ++r)

@@ -33,7 +33,7 @@ namespace fsa {
 template <int D, int NK>
 struct AttnCfg {
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(NK % 16 == 0 && NK >= 16 && NK <= 128, "key tile");
+    static_assert(NK % 16 == 0 && NK >= 16 && NK <= kMaxKeyTile(D), "key tile");
     static constexpr int BM = 128;                      // query rows per tile (MMA M)
     static constexpr int PANELS = D / 64;               // 64-element (128 B) swizzle panels
     static constexpr int Q_PANEL_BYTES = BM * 128;
@@ -68,9 +68,14 @@ struct AttnCfg {
     static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(KV_PANEL_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    // TMEM columns per query tile j: S_j (fp32, NK columns) followed by P_j (bf16 pairs, NK/2
+    // columns) inside a region of RS columns; then O_0 and O_1 (fp32, D columns each).
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t T_S = 0;      // + 128 * j
-    static constexpr uint32_t T_O = 256;    // + D * j
+    static constexpr uint32_t RS = ((NK + NK / 2) + 31) / 32 * 32;
+    static_assert(2 * RS + 2 * D <= TMEM_COLS, "TMEM budget");
+    static constexpr uint32_t t_s(int j) { return RS * j; }
+    static constexpr uint32_t t_p(int j) { return RS * j + NK; }
+    static constexpr uint32_t t_o(int j) { return 2 * RS + D * j; }
     static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NK, false, false);
     static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 };
@@ -202,44 +207,53 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------- MMA issuer
+        // Issue order per key tile t:  PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  While softmax 0
+        // works on S_0(t+1) the tensor pipe runs PV_1(t) and S_1(t+1), and the other way round,
+        // so the two query tiles keep the pipe busy in turn.  S_j(t+1) may overwrite S_j(t) as
+        // soon as P_j(t) is signalled (its softmax has read S_j(t) by then); P_j lives in its
+        // own columns, so it needs no wait for PV_j(t).
         if (lane == 0) {
+            auto issue_s = [&](int j, uint32_t k_s) {
+                const uint32_t q_s = sbase + C::Q_OFF + j * C::Q_TILE_BYTES;
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;  // 16 bf16 = 32 B inside the 128 B swizzle row
+                    const uint64_t a = smem_desc_sw128(q_s + (ks >> 2) * C::Q_PANEL_BYTES + off, 16, 1024);
+                    const uint64_t b = smem_desc_sw128(k_s + (ks >> 2) * C::KV_PANEL_BYTES + off, 16, 1024);
+                    mma_ss(tbase + C::t_s(j), a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
+                }
+                tc_commit(bar(C::B_SFULL + j));
+            };
             bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, SITE_MMA_Q);
-            tc_fence_after();
+            if (ok && n_tiles > 0) ok = mbar_wait(bar(C::B_KFULL), 0, wc, SITE_MMA_K);
+            if (ok && n_tiles > 0) {
+                tc_fence_after();
+                for (int j = 0; j < nq; ++j) issue_s(j, sbase + C::K_OFF);
+            }
             for (int t = 0; t < n_tiles && ok; ++t) {
                 const int st = t % C::NS;
-                const uint32_t ph = (t / C::NS) & 1;
-                if (!(ok = mbar_wait(bar(C::B_KFULL + st), ph, wc, SITE_MMA_K))) break;
-                tc_fence_after();
-                const uint32_t k_s = sbase + C::K_OFF + st * C::KV_TILE_BYTES;
+                const int st1 = (t + 1) % C::NS;
+                const bool next = t + 1 < n_tiles;
+                if (!(ok = mbar_wait(bar(C::B_VFULL + st), (t / C::NS) & 1, wc, SITE_MMA_V))) break;
                 const uint32_t v_s = sbase + C::V_OFF + st * C::KV_TILE_BYTES;
-                for (int j = 0; j < nq && ok; ++j) {
-                    if (t > 0) {
-                        if (!(ok = mbar_wait(bar(C::B_PVDONE + j), (t - 1) & 1, wc, SITE_MMA_PV))) break;
-                        tc_fence_after();
-                    }
-                    const uint32_t q_s = sbase + C::Q_OFF + j * C::Q_TILE_BYTES;
-#pragma unroll
-                    for (int ks = 0; ks < D / 16; ++ks) {
-                        const uint32_t off = (ks & 3) * 32;  // 16 bf16 = 32 B inside the 128 B swizzle row
-                        const uint64_t a = smem_desc_sw128(q_s + (ks >> 2) * C::Q_PANEL_BYTES + off, 16, 1024);
-                        const uint64_t b = smem_desc_sw128(k_s + (ks >> 2) * C::KV_PANEL_BYTES + off, 16, 1024);
-                        mma_ss(tbase + C::T_S + 128 * j, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
-                    }
-                    tc_commit(bar(C::B_SFULL + j));
-                }
-                if (!ok) break;
-                if (!(ok = mbar_wait(bar(C::B_VFULL + st), ph, wc, SITE_MMA_V))) break;
-                tc_fence_after();
                 for (int j = 0; j < nq && ok; ++j) {
                     if (!(ok = mbar_wait(bar(C::B_PFULL + j), t & 1, wc, SITE_MMA_P))) break;
                     tc_fence_after();
 #pragma unroll
                     for (int ks = 0; ks < NK / 16; ++ks) {
                         const uint64_t b = smem_desc_sw128(v_s + ks * 16 * 128, C::KV_PANEL_BYTES, 1024);
-                        mma_ts(tbase + C::T_O + D * j, tbase + C::T_S + 128 * j + ks * 8, b, C::IDESC_O,
+                        mma_ts(tbase + C::t_o(j), tbase + C::t_p(j) + ks * 8, b, C::IDESC_O,
                                (t > 0 || ks > 0) ? 1u : 0u);
                     }
                     tc_commit(bar(C::B_PVDONE + j));
+                    if (next) {
+                        if (j == 0) {
+                            if (!(ok = mbar_wait(bar(C::B_KFULL + st1), ((t + 1) / C::NS) & 1, wc, SITE_MMA_K)))
+                                break;
+                            tc_fence_after();
+                        }
+                        issue_s(j, sbase + C::K_OFF + st1 * C::KV_TILE_BYTES);
+                    }
                 }
                 if (!ok) break;
                 tc_commit(bar(C::B_KVEMPTY + st));
@@ -258,8 +272,9 @@ __global__ void __launch_bounds__(320, 1)
             const bool rv = row < valid;
             const int64_t grow = head_row0 + q_row0 + 128 * j + row;
             const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
-            const uint32_t tS = tbase + lane_off + C::T_S + 128 * j;
-            const uint32_t tO = tbase + lane_off + C::T_O + D * j;
+            const uint32_t tS = tbase + lane_off + C::t_s(j);
+            const uint32_t tP = tbase + lane_off + C::t_p(j);
+            const uint32_t tO = tbase + lane_off + C::t_o(j);
             const float c2 = rv ? p.scale_log2 : 0.0f;
             const float b_nat = (rv && p.bound) ? p.bound[grow] : 0.0f;
             const float nb2 = use_bound ? -b_nat * kLog2e : 0.0f;
@@ -272,42 +287,40 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 float s[NK];
                 tmem_load_cols<NK>(tS, s);
+                uint32_t pk[NK / 2];
+                float lp[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums: short add chains
+                float alpha = 1.0f, m_new = m2;
                 if (use_bound) {
 #pragma unroll
-                    for (int c = 0; c < NK / 16; ++c) {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float p0 = ex2(fmaf(s[16 * c + 2 * e], c2, nb2));
-                            const float p1 = ex2(fmaf(s[16 * c + 2 * e + 1], c2, nb2));
-                            pk[e] = pack_bf16x2(p0, p1);
-                            l += bf16_lo(pk[e]) + bf16_hi(pk[e]);  // normalise by the weights the MMA sees
-                        }
-                        tmem_st_x8(tS + 8 * c, pk);
+                    for (int e = 0; e < NK / 2; ++e) {
+                        const float p0 = ex2(fmaf(s[2 * e], c2, nb2));
+                        const float p1 = ex2(fmaf(s[2 * e + 1], c2, nb2));
+                        pk[e] = pack_bf16x2(p0, p1);
+                        lp[e & 3] += bf16_lo(pk[e]) + bf16_hi(pk[e]);  // normalise by the weights the MMA sees
                     }
                 } else {
-                    float mx = s[0];
+                    float mx[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-                    for (int i = 1; i < NK; ++i) mx = fmaxf(mx, s[i]);
-                    const float m_new = fmaxf(m2, mx * c2);
-                    const float alpha = ex2(m2 - m_new);
-                    float ls = 0.0f;
+                    for (int i = 4; i < NK; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
+                    m_new = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
+                    alpha = ex2(m2 - m_new);
 #pragma unroll
-                    for (int c = 0; c < NK / 16; ++c) {
-                        uint32_t pk[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float p0 = ex2(fmaf(s[16 * c + 2 * e], c2, -m_new));
-                            const float p1 = ex2(fmaf(s[16 * c + 2 * e + 1], c2, -m_new));
-                            pk[e] = pack_bf16x2(p0, p1);
-                            ls += bf16_lo(pk[e]) + bf16_hi(pk[e]);
-                        }
-                        tmem_st_x8(tS + 8 * c, pk);
+                    for (int e = 0; e < NK / 2; ++e) {
+                        const float p0 = ex2(fmaf(s[2 * e], c2, -m_new));
+                        const float p1 = ex2(fmaf(s[2 * e + 1], c2, -m_new));
+                        pk[e] = pack_bf16x2(p0, p1);
+                        lp[e & 3] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
                     }
-                    l = l * alpha + ls;
-                    // O holds P V through tile t-1 (S_j(t) was issued only after PV_j(t-1)
-                    // completed); rescale it before PV_j(t) may start.
-                    if (t > 0 && __any_sync(0xffffffffu, m_new > m2)) {
+                }
+                l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
+                if (t > 0) {
+                    // P_j and O_j are free again once PV_j(t-1) has completed
+                    if (!(ok = __all_sync(0xffffffffu,
+                                          mbar_wait(bar(C::B_PVDONE + j), (t - 1) & 1, wc, SITE_SOFT_O))))
+                        break;
+                    tc_fence_after();
+                    if (!use_bound && __any_sync(0xffffffffu, m_new > m2)) {
+                        // running max moved: rescale the accumulator before PV_j(t) may start
 #pragma unroll 1
                         for (int c = 0; c < D / 16; ++c) {
                             float o[16];
@@ -317,8 +330,10 @@ __global__ void __launch_bounds__(320, 1)
                             tmem_st_x16(tO + 16 * c, o);
                         }
                     }
-                    m2 = m_new;
                 }
+                m2 = m_new;
+#pragma unroll
+                for (int c = 0; c < NK / 16; ++c) tmem_st_x8(tP + 8 * c, pk + 8 * c);
                 tmem_st_wait();
                 tc_fence_before();
                 mbar_arrive(bar(C::B_PFULL + j));
@@ -409,8 +424,7 @@ int attn_smem_bytes(int D, int NK)
     if (D == d && NK == nk) return AttnCfg<d, nk>::SMEM_BYTES;
     FSA_SMEM_CASE(64, 16) FSA_SMEM_CASE(64, 32) FSA_SMEM_CASE(64, 48) FSA_SMEM_CASE(64, 64)
     FSA_SMEM_CASE(64, 80) FSA_SMEM_CASE(64, 96) FSA_SMEM_CASE(64, 112) FSA_SMEM_CASE(64, 128)
-    FSA_SMEM_CASE(128, 16) FSA_SMEM_CASE(128, 32) FSA_SMEM_CASE(128, 48) FSA_SMEM_CASE(128, 64)
-    FSA_SMEM_CASE(128, 80) FSA_SMEM_CASE(128, 96) FSA_SMEM_CASE(128, 112) FSA_SMEM_CASE(128, 128)
+    FSA_SMEM_CASE(128, 16) FSA_SMEM_CASE(128, 32) FSA_SMEM_CASE(128, 48) FSA_SMEM_CASE(128, 64) FSA_SMEM_CASE(128, 80)
 #undef FSA_SMEM_CASE
     return -1;
 }
@@ -421,8 +435,7 @@ int launch_attention(const AttnLaunch& L)
     if (L.D == d && L.NK == nk) return launch_attn<d, nk>(L);
     FSA_ATTN_CASE(64, 16) FSA_ATTN_CASE(64, 32) FSA_ATTN_CASE(64, 48) FSA_ATTN_CASE(64, 64)
     FSA_ATTN_CASE(64, 80) FSA_ATTN_CASE(64, 96) FSA_ATTN_CASE(64, 112) FSA_ATTN_CASE(64, 128)
-    FSA_ATTN_CASE(128, 16) FSA_ATTN_CASE(128, 32) FSA_ATTN_CASE(128, 48) FSA_ATTN_CASE(128, 64)
-    FSA_ATTN_CASE(128, 80) FSA_ATTN_CASE(128, 96) FSA_ATTN_CASE(128, 112) FSA_ATTN_CASE(128, 128)
+    FSA_ATTN_CASE(128, 16) FSA_ATTN_CASE(128, 32) FSA_ATTN_CASE(128, 48) FSA_ATTN_CASE(128, 64) FSA_ATTN_CASE(128, 80)
 #undef FSA_ATTN_CASE
     return -2;
 }

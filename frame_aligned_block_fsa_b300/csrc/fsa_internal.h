@@ -12,6 +12,10 @@ namespace fsa {
 // Key runs of one query frame: [n_runs, start_0, len_0, start_1, len_1, ...] in tokens of a
 // head; every run is a union of whole frames, ascending, disjoint.
 constexpr int kMaxRuns = 4;
+
+// Largest key tile the attention kernel supports for a head dim (TMEM budget: two query tiles
+// each hold S (NK fp32 columns) and P (NK/2 columns), plus two D-column accumulators).
+constexpr int kMaxKeyTile(int D) { return D == 128 ? 80 : 128; }
 constexpr int kRunStride = 1 + 2 * kMaxRuns;
 
 struct AttnParams {

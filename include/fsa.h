@@ -104,9 +104,10 @@ int fsa_plan_set_tau(fsa_plan_t plan, float tau);
 
 /*
  * fsa_plan_set_key_tile -- key rows per tensor-core tile: 0 = automatic (the largest
- * multiple of 16 that divides T and is <= 128), else a multiple of 16 in [16, 128]
- * dividing T.  Results are bitwise independent of `block`; they may change in the
- * last bits with the key tile (summation order).
+ * multiple of 16 that divides T and fits the kernel: at most 80 for D = 128, 128 for
+ * D = 64), else a multiple of 16 in [16, 128] dividing T; a tile above the limit for the
+ * call's D makes fsa_forward* return FSA_ERR_UNSUPPORTED.  Results are bitwise independent
+ * of `block`; they may change in the last bits with the key tile (summation order).
  */
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
 

@@ -120,6 +120,10 @@ def test_forward_rejects_bad_arguments_before_device_work(lib):
         assert lib.fsa_norms(fake, fake, 0, 64, h, None, None, None, None, None) == fsa.FSA_OK
         assert ex(*args(H=0, q=None, k=None, v=None, out=None, lse=None)) == fsa.FSA_OK
         assert lib.fsa_forward(fake, fake, fake, fake, fake, 2, 64, h, 7, None) == fsa.FSA_ERR_INVALID_ARG
+    # a key tile above the kernel's TMEM budget for D = 128 is refused before device work
+    with fsa.Plan(4, 256, 1, 0, 64) as p:
+        p.set_key_tile(128)
+        assert lib.fsa_forward(fake, fake, fake, fake, fake, 2, 128, p.handle, 0, None) == fsa.FSA_ERR_UNSUPPORTED
     # H * N beyond int32 row indexing
     with fsa.Plan(16, 3600, 1, 0, 144) as p:
         assert lib.fsa_forward(fake, fake, fake, fake, fake, 40000, 128, p.handle, 0, None) == \
