@@ -9,9 +9,10 @@ Public API (thin wrappers over the C ABI in include/fsa.h; every step runs in li
 
 The library is loaded lazily on first use; importing the package needs no GPU.
 """
-from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_TIMEOUT, FSA_ERR_UNSUPPORTED, FSA_OK,  # noqa: F401
-                   FsaError, Plan, forward, forward_ex, load, new_stats, norms, read_stats,
+from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_SCRATCH_LIMIT, FSA_ERR_TIMEOUT,  # noqa: F401
+                   FSA_ERR_UNSUPPORTED, FSA_OK,
+                   FsaError, Plan, forward, forward_ex, load, new_stats, norms, norms_noalloc, read_stats,
                    selftest_wait_timeout, status_string)
 
-__all__ = ["Plan", "norms", "forward", "forward_ex", "new_stats", "read_stats", "selftest_wait_timeout",
+__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "new_stats", "read_stats", "selftest_wait_timeout",
            "status_string", "load", "FsaError"]

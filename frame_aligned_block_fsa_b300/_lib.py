@@ -23,10 +23,12 @@ FSA_ERR_INVALID_ARG = -1
 FSA_ERR_UNSUPPORTED = -2
 FSA_ERR_CUDA = -3
 FSA_ERR_TIMEOUT = -4
+FSA_ERR_SCRATCH_LIMIT = -5
 
 # Exported symbols, in the order include/fsa.h declares them.
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
-           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_status_string", "fsa_selftest_wait_timeout")
+           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_norms_noalloc", "fsa_status_string",
+           "fsa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,6 +66,8 @@ def load():
             lib.fsa_forward.restype = i32
             lib.fsa_forward_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
             lib.fsa_forward_ex.restype = i32
+            lib.fsa_norms_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
+            lib.fsa_norms_noalloc.restype = i32
             lib.fsa_status_string.argtypes = [i32]
             lib.fsa_status_string.restype = ctypes.c_char_p
             lib.fsa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int32), vp]
@@ -173,6 +177,14 @@ def norms(q, k, plan: Plan, qnorm=None, kmax=None, bound=None, eligible=None, st
     st = _stream_handle(stream)
     _check("fsa_norms", load().fsa_norms(_ptr(q), _ptr(k), H, D, plan.handle, _ptr(qnorm), _ptr(kmax),
                                          _ptr(bound), _ptr(eligible), st))
+
+
+def norms_noalloc(q, k, plan: Plan, kmax, bound, eligible, qnorm=None, stream=None):
+    """fsa_norms_noalloc: fsa_norms without any device allocation (fixed in-library scratch)."""
+    H, N, D = _check_qkv(plan, q, k)
+    st = _stream_handle(stream)
+    _check("fsa_norms_noalloc", load().fsa_norms_noalloc(_ptr(q), _ptr(k), H, D, plan.handle, _ptr(qnorm),
+                                                         _ptr(kmax), _ptr(bound), _ptr(eligible), st))
 
 
 def forward(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=None, stream=None):

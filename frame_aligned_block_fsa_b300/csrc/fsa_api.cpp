@@ -187,6 +187,17 @@ int run_norms(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, int H, int D,
 
 }  // namespace
 
+int fsa::plan_view(const fsa_plan_s* P, PlanView* out)
+{
+    if (!P || !out) return FSA_ERR_INVALID_ARG;
+    out->F = P->F;
+    out->T = P->T;
+    out->N = P->N;
+    out->tau = P->tau;
+    out->runs = P->runs.data();
+    return FSA_OK;
+}
+
 extern "C" {
 
 const char* fsa_status_string(int status)
@@ -197,6 +208,7 @@ const char* fsa_status_string(int status)
         case FSA_ERR_UNSUPPORTED: return "unsupported";
         case FSA_ERR_CUDA: return "cuda error";
         case FSA_ERR_TIMEOUT: return "device wait timed out";
+        case FSA_ERR_SCRATCH_LIMIT: return "problem too large for the fixed no-allocation scratch";
         default: return "unknown status";
     }
 }

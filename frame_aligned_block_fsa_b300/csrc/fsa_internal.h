@@ -65,4 +65,14 @@ struct NormsLaunch {
 
 int launch_norms(const NormsLaunch& L);
 
+// Read-only view of a plan's host data, for entry points that live outside fsa_api.cpp.
+struct PlanView {
+    int F, T;
+    int64_t N;
+    float tau;
+    const int32_t* runs;  // host [F][kRunStride]
+};
+
+int plan_view(const fsa_plan_s* plan, PlanView* out);
+
 }  // namespace fsa

@@ -1,0 +1,108 @@
+// fsa_norms_noalloc.cu -- fsa_norms for callers that must not allocate device memory.
+//
+// fsa_norms keeps its scratch (per-frame key sums, per-head gap maxima) in a plan-owned
+// workspace that it grows with cudaMalloc.  Some callers cannot allow that: code that runs
+// while a CUDA graph is being captured, engines that own the whole device memory budget and
+// hand every buffer out themselves, and latency-critical loops that cannot afford the device
+// synchronisation cudaMalloc/cudaFree imply.  fsa_norms_noalloc runs the same three kernels
+// with that scratch in one file-scope device array of fixed size instead.
+//
+// The array is part of the library image: every GPU that loads the library holds it
+// (kNoAllocScratchBytes) until the process exits.  Host code cannot use the array's name as a
+// device address (on the host it names a host-side stand-in), so the first call on each device
+// looks the address up with cudaGetSymbolAddress, with that device current, and caches it.
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+
+#include "fsa.h"
+#include "fsa_internal.h"
+
+namespace fsa {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(2) << 20;  // 2 MiB
+
+static __device__ __align__(256) unsigned char g_norms_scratch[kNoAllocScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Device address of the scratch array on the current device (looked up once per device).
+int scratch_on_current_device(void** out)
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FSA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return FSA_ERR_UNSUPPORTED;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    if (major != 10 || minor != 3) return FSA_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_norms_scratch) != cudaSuccess || p == nullptr) return FSA_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return FSA_OK;
+}
+
+}  // namespace
+}  // namespace fsa
+
+extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t plan,
+                                 float* qnorm, float* kmax, float* bound, uint8_t* eligible, void* stream)
+{
+    fsa::PlanView pv;
+    if (fsa::plan_view(plan, &pv) != FSA_OK || H < 0) return FSA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return FSA_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(H) * pv.N >= (int64_t(1) << 31)) return FSA_ERR_INVALID_ARG;
+    if (H == 0) return FSA_OK;
+    if (!q || !k || !kmax || !bound || !eligible) return FSA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return FSA_ERR_INVALID_ARG;
+
+    // scratch layout: key runs of every query frame | per-frame key sums | per-head gap maxima
+    const size_t runs_bytes = static_cast<size_t>(pv.F) * fsa::kRunStride * sizeof(int32_t);
+    const size_t off_ksum = fsa::round256(runs_bytes);
+    const size_t ksum_bytes = static_cast<size_t>(H) * pv.F * D * sizeof(float);
+    const size_t off_gmax = off_ksum + fsa::round256(ksum_bytes);
+    const size_t total = off_gmax + fsa::round256(static_cast<size_t>(H) * sizeof(unsigned));
+    if (total > fsa::kNoAllocScratchBytes) return FSA_ERR_SCRATCH_LIMIT;
+
+    void* base = nullptr;
+    int rc = fsa::scratch_on_current_device(&base);
+    if (rc != FSA_OK) return rc;
+    unsigned char* s = static_cast<unsigned char*>(base);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The previous call's contents are overwritten: the runs here, the key sums by the first
+    // kernel, and the gap maxima are zeroed by the first kernel before the second max-reduces.
+    if (cudaMemcpyAsync(s, pv.runs, runs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return FSA_ERR_CUDA;
+
+    fsa::NormsLaunch L;
+    L.q = q;
+    L.k = k;
+    L.H = H;
+    L.D = D;
+    L.F = pv.F;
+    L.T = pv.T;
+    L.N = static_cast<int>(pv.N);
+    L.runs = reinterpret_cast<const int32_t*>(s);
+    L.scale = 1.0f / sqrtf(static_cast<float>(D));
+    L.tau = pv.tau;
+    L.qnorm = qnorm;
+    L.kmax = kmax;
+    L.ksum = reinterpret_cast<float*>(s + off_ksum);
+    L.bound = bound;
+    L.gmax = reinterpret_cast<unsigned*>(s + off_gmax);
+    L.eligible = eligible;
+    L.stream = st;
+    rc = fsa::launch_norms(L);
+    return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}

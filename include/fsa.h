@@ -50,7 +50,8 @@ enum fsa_status {
     FSA_ERR_INVALID_ARG = -1, /* bad shape, null pointer, block does not tile the frames */
     FSA_ERR_UNSUPPORTED = -2, /* D not in {64,128}, device is not sm_103, plan shape not handled */
     FSA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
-    FSA_ERR_TIMEOUT = -4      /* a bounded device-side wait gave up (reported via fsa_stats_t) */
+    FSA_ERR_TIMEOUT = -4,     /* a bounded device-side wait gave up (reported via fsa_stats_t) */
+    FSA_ERR_SCRATCH_LIMIT = -5 /* fsa_norms_noalloc: the problem needs more than its fixed scratch */
 };
 
 /* Device-side statistics, written by fsa_forward_ex when the caller passes a
@@ -157,6 +158,31 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
                    int H, int D, fsa_plan_t plan, int mode,
                    const float* bound, const uint8_t* eligible, float* rowmax,
                    fsa_stats_t* dev_stats, void* stream);
+
+/*
+ * fsa_norms_noalloc -- fsa_norms for callers that cannot allocate device memory.
+ * The pages have no counterpart; this is a service of the library.  fsa_norms keeps its
+ * scratch (per-frame key sums, per-head maxima) in a plan workspace grown with cudaMalloc,
+ * and its first call uploads the plan's work list.  Code that runs during CUDA graph
+ * capture, engines that hand out all device memory themselves, and loops that cannot afford
+ * the device synchronisation of cudaMalloc/cudaFree need a call that allocates nothing:
+ * this one keeps that scratch in a fixed 2 MiB device array compiled into the library (every
+ * GPU that loads the library holds it until the process exits) and copies the plan's key runs
+ * into it on every call (a small host-to-device copy on `stream`).
+ *   Arguments and results are those of fsa_norms, except that kmax, bound and eligible are
+ *   required (they are the outputs; qnorm may be NULL).
+ *   Limit: F*9*4 + H*F*D*4 + H*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
+ *   H=24, F=24, D=128 uses 0.3 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT before any
+ *   device work.
+ *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Every call shares the one array and overwrites what the previous call left there, so
+ *   calls whose work overlaps on the GPU (different streams, or different host threads) race;
+ *   serialise them.
+ *   Calls no cudaMalloc, cudaFree or other allocating routine.
+ */
+int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t plan,
+                      float* qnorm, float* kmax, float* bound, uint8_t* eligible, void* stream);
 
 /* Human-readable name of a status code (static storage). */
 const char* fsa_status_string(int status);
