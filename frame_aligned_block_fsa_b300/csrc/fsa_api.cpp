@@ -51,13 +51,6 @@ int cuda_status(cudaError_t e) { return e == cudaSuccess ? FSA_OK : FSA_ERR_CUDA
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Largest multiple of 16 that divides T and fits the kernel's TMEM budget for this D.
-int auto_key_tile(int T, int D)
-{
-    for (int nk = fsa::kMaxKeyTile(D); nk >= 16; nk -= 16)
-        if (T % nk == 0) return nk;
-    return 0;
-}
 
 int check_device()
 {
@@ -362,7 +355,7 @@ int fsa_plan_set_tau(fsa_plan_t plan, float tau)
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile)
 {
     if (!plan) return FSA_ERR_INVALID_ARG;
-    if (key_tile != 0 && (key_tile < 16 || key_tile > 128 || key_tile % 16 != 0 || plan->T % key_tile != 0))
+    if (key_tile != 0 && (key_tile < 16 || key_tile > 128 || key_tile % 16 != 0))
         return FSA_ERR_INVALID_ARG;
     plan->key_tile = key_tile;
     return FSA_OK;
@@ -392,13 +385,8 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
     if (H == 0) return FSA_OK;  // empty problem: nothing to read or write
     if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FSA_ERR_INVALID_ARG;
-    const int NK = plan->key_tile ? plan->key_tile : auto_key_tile(plan->T, D);
-    if (NK == 0 || NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
-    for (int f = 0; f < plan->F; ++f) {
-        const int32_t* R = &plan->runs[static_cast<size_t>(f) * kRunStride];
-        for (int r = 0; r < R[0]; ++r)
-            if (R[2 + 2 * r] % NK != 0) return FSA_ERR_UNSUPPORTED;
-    }
+    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile(D);
+    if (NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::lock_guard<std::mutex> lock(plan->mu);
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
@@ -410,18 +398,17 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
         eligible = plan->d_elig;
     }
     const int64_t rows = static_cast<int64_t>(H) * plan->N;
-    CUtensorMap mq, mk, mv;
-    if ((rc = make_tensor_map(&mq, q, rows, D, 128)) != FSA_OK) return rc;
+    CUtensorMap mk, mv;
     if ((rc = make_tensor_map(&mk, k, rows, D, NK)) != FSA_OK) return rc;
     if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
     fsa::AttnLaunch L;
     L.D = D;
     L.NK = NK;
     L.H = H;
-    L.tmQ = &mq;
     L.tmK = &mk;
     L.tmV = &mv;
     L.stream = st;
+    L.params.q = q;
     L.params.items = plan->d_items;
     L.params.runs = plan->d_runs;
     L.params.n_items = plan->n_items;

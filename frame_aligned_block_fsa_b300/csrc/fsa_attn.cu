@@ -10,16 +10,35 @@
 //    p = exp(s - b_i) needs no rescale of the accumulator; heads that fail the eligibility
 //    test take the running-max path inside the same kernel.
 //
-// B300 design (one CTA per SM, 10 warps):
-//   warp 8      TMA producer: the CTA's two 128-row query tiles once, then K and V tiles of
-//               NK keys through an NS-stage mbarrier ring (128-byte swizzled boxes).
-//   warp 9      allocates TMEM and issues tcgen05.mma from one thread:
-//                 S_j = Q_j K^T   (A, B from shared memory, fp32 accumulators in TMEM)
-//                 O_j += P_j V    (A = P from TMEM, B = V from shared memory, MN-major)
-//   warps 0-3   softmax + epilogue for query tile 0 (thread = row = TMEM lane)
-//   warps 4-7   the same for query tile 1 (same frame, next 128 rows)
-// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,256+D), O_1 [256+D,256+2D);
-// P_j (bf16) overwrites the first NK/2 columns of S_j.
+// B300 design (one CTA per SM, 18 warps, two 128-row query tiles j = 0, 1 of one frame):
+//   warps 0-7   query tile 0: load Q_0 into TMEM once, then per key tile the softmax and at
+//               the end the epilogue.  A thread owns one row (= TMEM lane); the two warps
+//               of a lane quarter (w and w + 4) split the key tile's 16-column chunks
+//               (even / odd), so a row's exponentials run in two warps at once.
+//   warps 8-15  the same for query tile 1
+//   warp 16     TMA producer: K and V tiles of up to NK keys through an NS-stage mbarrier
+//               ring (128-byte swizzled boxes)
+//   warp 17     allocates TMEM and issues tcgen05.mma (the warp runs the loop, one elected
+//               lane issues):
+//                 S_j  = Q_j K^T   (A = Q_j from TMEM, B = K tile from shared memory)
+//                 O_j += P_j V     (A = P_j from TMEM, B = V tile from shared memory, MN-major)
+// The tensor pipe takes MMAs from a very short queue: an issuing thread stays blocked for
+// about as long as its MMAs take, and the pipe idles while the issuer waits.
+// Both products take A from TMEM.  With A in shared memory a 128 x 80 x 16 MMA reads 6.5 KB
+// of operands for 40 cycles of math, more than shared memory delivers (128 B/clk), which
+// slowed the MMAs and every other shared-memory access of the CTA, barriers included.
+//
+// TMEM (512 columns): per query tile j a 256-column region
+//   [S_j: NK fp32 columns][Q_j: D/2][O_j: D fp32].
+// P_j(t) overwrites S_j(t) after the softmax has read it: the 8 bf16-pair columns of the 16
+// keys of S chunk c go to the first 8 columns of that chunk, so each warp overwrites only
+// columns it has read itself.  S_j(t+1) is issued after PV_j(t) by the same thread, and the
+// tensor pipe executes one thread's MMAs in issue order, so PV_j(t) has read P_j(t) before
+// S_j(t+1) overwrites it.
+//
+// Key tiles: each key run (a whole number of frames) is cut into tiles of NK keys and one
+// last narrower tile of the remaining len mod NK keys (a multiple of 16, since T is).  Every
+// tile is fully inside the mask; a narrower tile is an MMA of smaller N (S) or K (PV).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -30,60 +49,59 @@
 
 namespace fsa {
 
+constexpr int kAttnThreads = 576;  // 16 softmax warps, the TMA warp, the MMA warp
+constexpr int kWarpTma = 16, kWarpMma = 17;
+
 template <int D, int NK>
 struct AttnCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static_assert(NK % 16 == 0 && NK >= 16 && NK <= kMaxKeyTile(D), "key tile");
     static constexpr int BM = 128;                      // query rows per tile (MMA M)
     static constexpr int PANELS = D / 64;               // 64-element (128 B) swizzle panels
-    static constexpr int Q_PANEL_BYTES = BM * 128;
-    static constexpr int Q_TILE_BYTES = BM * D * 2;
     static constexpr int KV_PANEL_BYTES = NK * 128;
     static constexpr int KV_TILE_BYTES = NK * D * 2;
     static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;  // K and V
     static constexpr int SMEM_LIMIT = 232448;              // max dynamic smem per block
     static constexpr int RESERVED = 256;                   // barriers + flags
-    static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - RESERVED - 2 * Q_TILE_BYTES) / STAGE_BYTES;
-    static constexpr int NS = NS_FIT < 4 ? NS_FIT : 4;
+    static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - RESERVED) / STAGE_BYTES;
+    static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
     static_assert(NS >= 2, "pipeline depth");
-    static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = 2 * Q_TILE_BYTES;
+    static constexpr int K_OFF = 0;
     static constexpr int V_OFF = K_OFF + NS * KV_TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + NS * KV_TILE_BYTES;
     // barrier indices
-    static constexpr int B_QFULL = 0;
-    static constexpr int B_KFULL = 1;
-    static constexpr int B_VFULL = B_KFULL + NS;
-    static constexpr int B_KVEMPTY = B_VFULL + NS;
-    static constexpr int B_SFULL = B_KVEMPTY + NS;  // 2
-    static constexpr int B_PFULL = B_SFULL + 2;     // 2
-    static constexpr int B_PVDONE = B_PFULL + 2;    // 2
+    static constexpr int B_KVFULL = 0;                // NS: K and V of a stage landed
+    static constexpr int B_KVEMPTY = B_KVFULL + NS;   // NS: the MMAs reading a stage are done
+    static constexpr int B_SFULL = B_KVEMPTY + NS;    // 2: S_j complete (and every MMA before it)
+    static constexpr int B_PVDONE = B_SFULL + 2;      // 2: the last PV_j complete
     static constexpr int B_DRAIN = B_PVDONE + 2;
     static constexpr int N_BARS = B_DRAIN + 1;
-    static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;  // abort flag, TMEM address
-    static_assert(MISC_OFF + 16 <= BAR_OFF + RESERVED, "reserved area");
-    static constexpr int SMEM_USED = 1024 + BAR_OFF + RESERVED;
+    // abort flag (+0), TMEM address (+8), ready counters of the two query tiles (+16, +20),
+    // row-sum exchange counters (+24, +28)
+    static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
+    static_assert(MISC_OFF + 32 <= BAR_OFF + RESERVED, "reserved area");
+    // per query tile, per column half, per row: the half's partial row sum (epilogue)
+    static constexpr int LSUM_OFF = BAR_OFF + RESERVED;
+    static constexpr int SMEM_USED = 1024 + LSUM_OFF + 2 * 2 * 128 * 4;
     // At least half of the SM's shared memory, so two CTAs never share an SM and contend for
     // its 512 TMEM columns.
     static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
     static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
     static_assert(KV_PANEL_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
-    // TMEM columns per query tile j: S_j (fp32, NK columns) followed by P_j (bf16 pairs, NK/2
-    // columns) inside a region of RS columns; then O_0 and O_1 (fp32, D columns each).
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t RS = ((NK + NK / 2) + 31) / 32 * 32;
-    static_assert(2 * RS + 2 * D <= TMEM_COLS, "TMEM budget");
-    static constexpr uint32_t t_s(int j) { return RS * j; }
-    static constexpr uint32_t t_p(int j) { return RS * j + NK; }
-    static constexpr uint32_t t_o(int j) { return 2 * RS + D * j; }
-    static constexpr uint32_t IDESC_S = idesc_bf16_f32(128, NK, false, false);
+    static constexpr uint32_t REGION = 256;
+    static_assert(NK + D / 2 + D <= static_cast<int>(REGION), "TMEM budget");
+    static constexpr uint32_t t_s(int j) { return REGION * j; }
+    static constexpr uint32_t t_p(int j) { return REGION * j; }  // chunk c's P at t_p + 16 c
+    static constexpr uint32_t t_q(int j) { return REGION * j + NK; }
+    static constexpr uint32_t t_o(int j) { return REGION * j + NK + D / 2; }
     static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 };
 
 // wait sites (diagnostic codes in fsa_stats_t::timeout_site)
 enum : int {
-    SITE_PROD_EMPTY = 1, SITE_MMA_Q = 2, SITE_MMA_K = 3, SITE_MMA_PV = 4, SITE_MMA_V = 5,
-    SITE_MMA_P = 6, SITE_SOFT_S = 7, SITE_SOFT_O = 8, SITE_DRAIN = 9, SITE_SELFTEST = 10
+    SITE_PROD_EMPTY = 1, SITE_MMA_K = 3, SITE_MMA_Q = 4, SITE_MMA_P = 6, SITE_SOFT_S = 7, SITE_SOFT_O = 8,
+    SITE_DRAIN = 9, SITE_SELFTEST = 10
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -102,10 +120,29 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* v)
     for (int i = 0; i < W; ++i) reg_fence(v[i]);
 }
 
+// Walks a query frame's key runs in tiles of at most NK keys: (first key, width).
+template <int NK>
+struct KeyTiles {
+    const int32_t* runs;
+    int r = 0, k0 = 0;
+    __device__ explicit KeyTiles(const int32_t* rr) : runs(rr) {}
+    __device__ __forceinline__ void next(int& start, int& width)
+    {
+        const int len = runs[2 + 2 * r];
+        start = runs[1 + 2 * r] + k0;
+        width = min(NK, len - k0);
+        k0 += width;
+        if (k0 == len) {
+            k0 = 0;
+            ++r;
+        }
+    }
+};
+
 template <int D, int NK>
-__global__ void __launch_bounds__(320, 1)
-    fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                        const __grid_constant__ CUtensorMap tmV, const AttnParams p)
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const AttnParams p)
 {
     using C = AttnCfg<D, NK>;
     extern __shared__ uint8_t smem_raw[];
@@ -115,6 +152,10 @@ __global__ void __launch_bounds__(320, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::MISC_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
+    uint32_t* ready = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 16);
+    // ready[j] counts warp signals of query tile j: 8 once Q_j is in TMEM, then 8 more per
+    // key tile t once P_j(t) is in TMEM.
+    auto ready_addr = [&](int j) -> uint32_t { return sbase + C::MISC_OFF + 16u + 4u * static_cast<uint32_t>(j); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -126,30 +167,29 @@ __global__ void __launch_bounds__(320, 1)
     const int32_t* runs = p.runs + f * kRunStride;
     const int n_runs = runs[0];
     int n_tiles = 0;
-    for (int r = 0; r < n_runs; ++r) n_tiles += runs[2 + 2 * r] / NK;
+    for (int r = 0; r < n_runs; ++r) n_tiles += (runs[2 + 2 * r] + NK - 1) / NK;
     const int64_t head_row0 = static_cast<int64_t>(h) * p.N;
 
     const bool use_bound = (p.mode == 0) && (p.bound != nullptr) &&
                            (p.eligible == nullptr || p.eligible[h] != 0);
 
     if (threadIdx.x == 0) {
-        mbar_init(bar(C::B_QFULL), 1);
         for (int s = 0; s < C::NS; ++s) {
-            mbar_init(bar(C::B_KFULL + s), 1);
-            mbar_init(bar(C::B_VFULL + s), 1);
+            mbar_init(bar(C::B_KVFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
         for (int j = 0; j < 2; ++j) {
             mbar_init(bar(C::B_SFULL + j), 1);
-            mbar_init(bar(C::B_PFULL + j), 128);
             mbar_init(bar(C::B_PVDONE + j), 1);
+            ready[j] = 0;
+            ready[2 + j] = 0;
         }
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
         fence_mbar_init();
         if (p.stats && item == 0 && p.mode == 0 && !use_bound) atomicAdd(&p.stats->fallback_heads, 1);
     }
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -164,109 +204,138 @@ __global__ void __launch_bounds__(320, 1)
     wc.err_site = p.stats ? &p.stats->timeout_site : nullptr;
     wc.limit = p.wait_limit;
 
-    if (warp == 8) {
+    if (warp == kWarpTma) {
         // ------------------------------------------------------------- TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             const uint64_t pol_kv = policy_evict_last();
-            mbar_arrive_expect_tx(bar(C::B_QFULL), static_cast<uint32_t>(nq * C::Q_TILE_BYTES));
-            for (int j = 0; j < nq; ++j)
-                for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_2d(sbase + C::Q_OFF + j * C::Q_TILE_BYTES + pn * C::Q_PANEL_BYTES, &tmQ,
-                                pn * 64, static_cast<int>(head_row0 + q_row0 + j * 128), bar(C::B_QFULL));
+            KeyTiles<NK> tiles(runs);
             int t = 0;
-            bool ok = true;
-            for (int r = 0; r < n_runs && ok; ++r) {
-                const int start = runs[1 + 2 * r];
-                const int len = runs[2 + 2 * r];
-                for (int k0 = 0; k0 < len; k0 += NK, ++t) {
-                    const int st = t % C::NS;
-                    if (!mbar_wait(bar(C::B_KVEMPTY + st), ((t / C::NS) & 1) ^ 1, wc, SITE_PROD_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    const int row = static_cast<int>(head_row0 + start + k0);
-                    mbar_arrive_expect_tx(bar(C::B_KFULL + st), C::KV_TILE_BYTES);
-                    for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_2d_hint(sbase + C::K_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES,
-                                         &tmK, pn * 64, row, bar(C::B_KFULL + st), pol_kv);
-                    mbar_arrive_expect_tx(bar(C::B_VFULL + st), C::KV_TILE_BYTES);
-                    for (int pn = 0; pn < C::PANELS; ++pn)
-                        tma_load_2d_hint(sbase + C::V_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES,
-                                         &tmV, pn * 64, row, bar(C::B_VFULL + st), pol_kv);
-                }
+            for (; t < n_tiles; ++t) {
+                const int st = t % C::NS;
+                if (!mbar_wait(bar(C::B_KVEMPTY + st), ((t / C::NS) & 1) ^ 1, wc, SITE_PROD_EMPTY)) break;
+                int start, width;
+                tiles.next(start, width);
+                // A narrower last tile still loads a full box: the rows past it are never read
+                // by the MMAs (rows past the tensor are zero-filled).
+                const int row = static_cast<int>(head_row0 + start);
+                mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::KV_TILE_BYTES);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_2d_hint(sbase + C::K_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES, &tmK,
+                                     pn * 64, row, bar(C::B_KVFULL + st), pol_kv);
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_2d_hint(sbase + C::V_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES, &tmV,
+                                     pn * 64, row, bar(C::B_KVFULL + st), pol_kv);
             }
             // Every copy this thread issued must land before the CTA may exit.
-            mbar_wait(bar(C::B_QFULL), 0, wc, SITE_DRAIN, false);
-            for (int u = (t > C::NS ? t - C::NS : 0); u < t; ++u) {
-                mbar_wait(bar(C::B_KFULL + u % C::NS), (u / C::NS) & 1, wc, SITE_DRAIN, false);
-                mbar_wait(bar(C::B_VFULL + u % C::NS), (u / C::NS) & 1, wc, SITE_DRAIN, false);
-            }
+            for (int u = (t > C::NS ? t - C::NS : 0); u < t; ++u)
+                mbar_wait(bar(C::B_KVFULL + u % C::NS), (u / C::NS) & 1, wc, SITE_DRAIN, false);
         }
-    } else if (warp == 9) {
+    } else if (warp == kWarpMma) {
         // ------------------------------------------------------------- MMA issuer
-        // Issue order per key tile t:  PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  While softmax 0
-        // works on S_0(t+1) the tensor pipe runs PV_1(t) and S_1(t+1), and the other way round,
-        // so the two query tiles keep the pipe busy in turn.  S_j(t+1) may overwrite S_j(t) as
-        // soon as P_j(t) is signalled (its softmax has read S_j(t) by then); P_j lives in its
-        // own columns, so it needs no wait for PV_j(t).
-        if (lane == 0) {
-            auto issue_s = [&](int j, uint32_t k_s) {
-                const uint32_t q_s = sbase + C::Q_OFF + j * C::Q_TILE_BYTES;
+        // Issue order per key tile t:  PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  While softmax j
+        // works on S_j(t+1) the pipe runs the other query tile's pair, so the two tiles keep
+        // the pipe busy in turn.  A commit arrives when every MMA its thread issued before it
+        // has completed, so S_j(t+1) being complete also means PV_j(t) is: P_j and O_j are
+        // free for the softmax.
+        //
+        // The whole warp runs the loop, so the waits and the descriptor arithmetic stay
+        // warp-uniform; one elected lane issues every tcgen05.mma and tcgen05.commit (a commit
+        // tracks the MMAs of its own thread, so the same lane issues all of them).  The next
+        // K/V stage's barrier is tested a tile ahead; the softmax hand-off is a shared counter.
+        const bool leader = elect_one();
+        // Descriptor bases; moving the start address by b bytes adds b >> 4 to the descriptor.
+        const uint64_t dk = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
+        const uint64_t dv = smem_desc_sw128(sbase + C::V_OFF, C::KV_PANEL_BYTES, 1024);
+        // S_j = Q_j K^T over the stage's keys (`probe` would run after half of the MMAs).
+        auto issue_s = [&](int j, int st, int width, auto&& probe) {
+            const uint64_t b0 = dk + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
+            const uint32_t idesc = idesc_bf16_f32(128, width, false, false);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks & 3) * 32;  // 16 bf16 = 32 B inside the 128 B swizzle row
-                    const uint64_t a = smem_desc_sw128(q_s + (ks >> 2) * C::Q_PANEL_BYTES + off, 16, 1024);
-                    const uint64_t b = smem_desc_sw128(k_s + (ks >> 2) * C::KV_PANEL_BYTES + off, 16, 1024);
-                    mma_ss(tbase + C::t_s(j), a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
-                }
-                tc_commit(bar(C::B_SFULL + j));
-            };
-            bool ok = mbar_wait(bar(C::B_QFULL), 0, wc, SITE_MMA_Q);
-            if (ok && n_tiles > 0) ok = mbar_wait(bar(C::B_KFULL), 0, wc, SITE_MMA_K);
-            if (ok && n_tiles > 0) {
-                tc_fence_after();
-                for (int j = 0; j < nq; ++j) issue_s(j, sbase + C::K_OFF);
+            for (int ks = 0; ks < D / 16; ++ks) {
+                if (ks == D / 32) probe();
+                // 16 bf16 = 32 B inside the 128 B swizzle row; a new 64-column panel every 4 steps
+                const uint32_t ko = ((ks >> 2) * C::KV_PANEL_BYTES + (ks & 3) * 32) >> 4;
+                if (leader) mma_ts(tbase + C::t_s(j), tbase + C::t_q(j) + ks * 8, b0 + ko, idesc, ks > 0 ? 1u : 0u);
             }
-            for (int t = 0; t < n_tiles && ok; ++t) {
-                const int st = t % C::NS;
-                const int st1 = (t + 1) % C::NS;
-                const bool next = t + 1 < n_tiles;
-                if (!(ok = mbar_wait(bar(C::B_VFULL + st), (t / C::NS) & 1, wc, SITE_MMA_V))) break;
-                const uint32_t v_s = sbase + C::V_OFF + st * C::KV_TILE_BYTES;
-                for (int j = 0; j < nq && ok; ++j) {
-                    if (!(ok = mbar_wait(bar(C::B_PFULL + j), t & 1, wc, SITE_MMA_P))) break;
-                    tc_fence_after();
+            if (leader) tc_commit(bar(C::B_SFULL + j));
+            __syncwarp();
+        };
+        auto issue_pv = [&](int j, int st, int width, bool first, bool last) {
+            const uint64_t b0 = dv + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
+            if (leader) {
 #pragma unroll
-                    for (int ks = 0; ks < NK / 16; ++ks) {
-                        const uint64_t b = smem_desc_sw128(v_s + ks * 16 * 128, C::KV_PANEL_BYTES, 1024);
-                        mma_ts(tbase + C::t_o(j), tbase + C::t_p(j) + ks * 8, b, C::IDESC_O,
-                               (t > 0 || ks > 0) ? 1u : 0u);
-                    }
-                    tc_commit(bar(C::B_PVDONE + j));
-                    if (next) {
-                        if (j == 0) {
-                            if (!(ok = mbar_wait(bar(C::B_KFULL + st1), ((t + 1) / C::NS) & 1, wc, SITE_MMA_K)))
-                                break;
-                            tc_fence_after();
-                        }
-                        issue_s(j, sbase + C::K_OFF + st1 * C::KV_TILE_BYTES);
-                    }
-                }
-                if (!ok) break;
-                tc_commit(bar(C::B_KVEMPTY + st));
+                for (int ks = 0; ks < NK / 16; ++ks)
+                    if (ks < width / 16)
+                        mma_ts(tbase + C::t_o(j), tbase + C::t_p(j) + ks * 16, b0 + ((ks * 16 * 128) >> 4),
+                               C::IDESC_O, (!first || ks > 0) ? 1u : 0u);
+                if (last) tc_commit(bar(C::B_PVDONE + j));
             }
-            // Every MMA this thread issued must complete before TMEM is released.
-            tc_commit(bar(C::B_DRAIN));
-            mbar_wait(bar(C::B_DRAIN), 0, wc, SITE_DRAIN, false);
+            __syncwarp();
+        };
+        auto stage_wait = [&](int t, bool pretested) -> bool {
+            if (__all_sync(0xffffffffu, pretested)) return true;
+            return __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVFULL + t % C::NS), (t / C::NS) & 1, wc, SITE_MMA_K));
+        };
+        // readiness of query tile j for key tile t (Q_j and P_j(0..t) in TMEM)
+        auto p_target = [](int t) { return 8u * static_cast<uint32_t>(t + 2); };
+        auto p_wait = [&](int j, int t, bool seen) -> bool {
+            if (__all_sync(0xffffffffu, seen)) return true;
+            return __all_sync(0xffffffffu, counter_wait(ready_addr(j), p_target(t), wc, SITE_MMA_P));
+        };
+        auto no_probe = [] {};
+        KeyTiles<NK> tiles(runs);
+        int start, w_cur = 0, w_next = 0;
+        bool ok = n_tiles > 0;
+        if (ok) {
+            tiles.next(start, w_cur);
+            ok = stage_wait(0, false);
         }
+        for (int j = 0; j < nq && ok; ++j) {
+            if (!(ok = __all_sync(0xffffffffu, counter_wait(ready_addr(j), 8u, wc, SITE_MMA_Q)))) break;
+            tc_fence_after();
+            issue_s(j, 0, w_cur, no_probe);
+        }
+        bool next_ready = false;  // answer of an early test of the stage of tile t+1
+        if (ok && n_tiles > 1) next_ready = mbar_test_wait(bar(C::B_KVFULL + 1 % C::NS), (1 / C::NS) & 1);
+        for (int t = 0; t < n_tiles && ok; ++t) {
+            const int st = t % C::NS;
+            const int st1 = (t + 1) % C::NS;
+            const bool next = t + 1 < n_tiles;
+            if (next) tiles.next(start, w_next);
+            bool ready2 = false;
+            for (int j = 0; j < nq && ok; ++j) {
+                if (!(ok = p_wait(j, t, false))) break;
+                tc_fence_after();
+                issue_pv(j, st, w_cur, t == 0, !next);
+                if (next) {
+                    if (j == 0) {
+                        if (!(ok = stage_wait(t + 1, next_ready))) break;
+                        tc_fence_after();
+                        if (t + 2 < n_tiles)
+                            ready2 = mbar_test_wait(bar(C::B_KVFULL + (t + 2) % C::NS), ((t + 2) / C::NS) & 1);
+                    }
+                    issue_s(j, st1, w_next, no_probe);
+                }
+            }
+            if (!ok) break;
+            next_ready = ready2;
+            w_cur = w_next;
+            if (leader) tc_commit(bar(C::B_KVEMPTY + st));
+            __syncwarp();
+        }
+        // Every MMA this warp issued must complete before TMEM is released.
+        if (leader) tc_commit(bar(C::B_DRAIN));
+        __syncwarp();
+        mbar_wait(bar(C::B_DRAIN), 0, wc, SITE_DRAIN, false);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax + epilogue
-        const int j = warp >> 2;
+        const int j = warp >> 3;
         if (j < nq) {
             const int quarter = warp & 3;
+            const int hf = (warp >> 2) & 1;  // this warp's chunks: c = 2 i + hf
             const int row = 32 * quarter + lane;
             const int valid = j == 0 ? valid0 : valid1;
             const bool rv = row < valid;
@@ -274,78 +343,132 @@ __global__ void __launch_bounds__(320, 1)
             const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
             const uint32_t tS = tbase + lane_off + C::t_s(j);
             const uint32_t tP = tbase + lane_off + C::t_p(j);
-            const uint32_t tO = tbase + lane_off + C::t_o(j);
+            const uint32_t tQ = tbase + lane_off + C::t_q(j);
+            const uint32_t tO = tbase + lane_off + C::t_o(j) + hf * (D / 2);  // this warp's half of O
+            constexpr int OWN = (NK / 16 + 1) / 2;  // most chunks a warp owns
+            // Q_j into TMEM: the row as D/2 columns of bf16 pairs (the layout of an MMA A
+            // operand in TMEM), this warp's half of them; rows past the frame's last token are 0.
+            {
+                const uint4* qrow = reinterpret_cast<const uint4*>(p.q + grow * D) + hf * (D / 16);
+#pragma unroll
+                for (int c = 0; c < D / 64; ++c) {
+                    uint32_t qw[16];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const uint4 u = rv ? __ldg(qrow + 4 * c + e) : make_uint4(0u, 0u, 0u, 0u);
+                        qw[4 * e] = u.x;
+                        qw[4 * e + 1] = u.y;
+                        qw[4 * e + 2] = u.z;
+                        qw[4 * e + 3] = u.w;
+                    }
+                    tmem_st_x8(tQ + hf * (D / 4) + 16 * c, qw);
+                    tmem_st_x8(tQ + hf * (D / 4) + 16 * c + 8, qw + 8);
+                }
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) red_release_shared_add(ready_addr(j), 1u);
+            }
             const float c2 = rv ? p.scale_log2 : 0.0f;
             const float b_nat = (rv && p.bound) ? p.bound[grow] : 0.0f;
             const float nb2 = use_bound ? -b_nat * kLog2e : 0.0f;
             float m2 = -INFINITY;  // running max in log2 units (online path)
-            float l = 0.0f;
+            float l = 0.0f;        // sum of this warp's weights of the row
             bool ok = true;
+            KeyTiles<NK> tiles(runs);
             for (int t = 0; t < n_tiles; ++t) {
+                int start, width;
+                tiles.next(start, width);
+                const int nch = width / 16;  // 16-column chunks of this tile
                 // the vote keeps the warp converged for the warp-collective TMEM accesses
                 if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + j), t & 1, wc, SITE_SOFT_S)))) break;
                 tc_fence_after();
-                float s[NK];
-                tmem_load_cols<NK>(tS, s);
-                uint32_t pk[NK / 2];
-                float lp[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // independent partial sums: short add chains
+                float s[16 * OWN];  // own chunks, compact
+                uint32_t pk[8 * OWN];
+#pragma unroll
+                for (int i = 0; i < OWN; ++i)
+                    if (2 * i + hf < nch) tmem_ld_x16(tS + 16 * (2 * i + hf), s + 16 * i);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16 * OWN; ++i) reg_fence(s[i]);
+                // Two packed partial sums of the fp32 weights (short add chains).
+                float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
                 float alpha = 1.0f, m_new = m2;
-                if (use_bound) {
+                float2 off = make_float2(nb2, nb2);
+                if (!use_bound) {
+                    // the running max over the whole row: both warps of the row compute it,
+                    // reading the other warp's chunks one at a time
+                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int e = 0; e < NK / 2; ++e) {
-                        const float p0 = ex2(fmaf(s[2 * e], c2, nb2));
-                        const float p1 = ex2(fmaf(s[2 * e + 1], c2, nb2));
-                        pk[e] = pack_bf16x2(p0, p1);
-                        lp[e & 3] += bf16_lo(pk[e]) + bf16_hi(pk[e]);  // normalise by the weights the MMA sees
+                    for (int i = 0; i < OWN; ++i) {
+                        if (2 * i + hf < nch) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[16 * i + e]);
+                        }
+                        if (2 * i + 1 - hf < nch) {
+                            float so[16];
+                            tmem_load_cols<16>(tS + 16 * (2 * i + 1 - hf), so);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) mx[e & 3] = fmaxf(mx[e & 3], so[e]);
+                        }
                     }
-                } else {
-                    float mx[4] = {s[0], s[1], s[2], s[3]};
-#pragma unroll
-                    for (int i = 4; i < NK; ++i) mx[i & 3] = fmaxf(mx[i & 3], s[i]);
                     m_new = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
                     alpha = ex2(m2 - m_new);
+                    off = make_float2(-m_new, -m_new);
+                }
+                const float2 cc = make_float2(c2, c2);
 #pragma unroll
-                    for (int e = 0; e < NK / 2; ++e) {
-                        const float p0 = ex2(fmaf(s[2 * e], c2, -m_new));
-                        const float p1 = ex2(fmaf(s[2 * e + 1], c2, -m_new));
-                        pk[e] = pack_bf16x2(p0, p1);
-                        lp[e & 3] += bf16_lo(pk[e]) + bf16_hi(pk[e]);
+                for (int i = 0; i < OWN; ++i) {
+                    if (2 * i + hf < nch) {
+#pragma unroll
+                        for (int e = 8 * i; e < 8 * i + 8; ++e) {
+                            const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cc, off);
+                            const float p0 = ex2(x.x);
+                            const float p1 = ex2(x.y);
+                            pk[e] = pack_bf16x2(p0, p1);
+                            acc[e & 1] = fadd2(acc[e & 1], make_float2(p0, p1));
+                        }
                     }
                 }
-                l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
-                if (t > 0) {
-                    // P_j and O_j are free again once PV_j(t-1) has completed
-                    if (!(ok = __all_sync(0xffffffffu,
-                                          mbar_wait(bar(C::B_PVDONE + j), (t - 1) & 1, wc, SITE_SOFT_O))))
-                        break;
-                    tc_fence_after();
-                    if (!use_bound && __any_sync(0xffffffffu, m_new > m2)) {
-                        // running max moved: rescale the accumulator before PV_j(t) may start
+                l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
+                // S_j(t) complete means PV_j(t-1) is too (issued before it): O_j may be
+                // rescaled and P_j(t) may overwrite S_j(t) now.
+                if (!use_bound && t > 0 && __any_sync(0xffffffffu, m_new > m2)) {
+                    // running max moved: rescale this warp's half of the accumulator before
+                    // PV_j(t) may start
 #pragma unroll 1
-                        for (int c = 0; c < D / 16; ++c) {
-                            float o[16];
-                            tmem_load_cols<16>(tO + 16 * c, o);
+                    for (int c = 0; c < D / 32; ++c) {
+                        float o[16];
+                        tmem_load_cols<16>(tO + 16 * c, o);
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) o[e] *= alpha;
-                            tmem_st_x16(tO + 16 * c, o);
-                        }
+                        for (int e = 0; e < 16; ++e) o[e] *= alpha;
+                        tmem_st_x16(tO + 16 * c, o);
                     }
                 }
                 m2 = m_new;
 #pragma unroll
-                for (int c = 0; c < NK / 16; ++c) tmem_st_x8(tP + 8 * c, pk + 8 * c);
+                for (int i = 0; i < OWN; ++i)
+                    if (2 * i + hf < nch) tmem_st_x8(tP + 16 * (2 * i + hf), pk + 8 * i);
                 tmem_st_wait();
                 tc_fence_before();
-                mbar_arrive(bar(C::B_PFULL + j));
+                __syncwarp();
+                if (lane == 0) red_release_shared_add(ready_addr(j), 1u);
             }
             if (ok && n_tiles > 0)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + j), (n_tiles - 1) & 1, wc, SITE_SOFT_O));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + j), 0, wc, SITE_SOFT_O));
+            // The row sum is split over the two warps of the row: exchange the halves.
+            float* lsum = reinterpret_cast<float*>(sgen + C::LSUM_OFF) + (2 * j) * 128;
+            lsum[hf * 128 + row] = l;
+            __syncwarp();
+            if (lane == 0) red_release_shared_add(ready_addr(2 + j), 1u);
+            if (ok) ok = __all_sync(0xffffffffu, counter_wait(ready_addr(2 + j), 8u, wc, SITE_SOFT_O));
             if (ok) {
                 tc_fence_after();
-                const float inv_l = 1.0f / l;
-                float* orow = p.out + grow * D;
+                const float l_row = l + lsum[(1 - hf) * 128 + row];
+                const float inv_l = 1.0f / l_row;
+                float* orow = p.out + grow * D + hf * (D / 2);
 #pragma unroll 1
-                for (int c = 0; c < D / 16; ++c) {
+                for (int c = 0; c < D / 32; ++c) {
                     float o[16];
                     tmem_load_cols<16>(tO + 16 * c, o);
                     if (rv) {
@@ -356,17 +479,20 @@ __global__ void __launch_bounds__(320, 1)
                                                  o[4 * e + 3] * inv_l);
                     }
                 }
-                const float m_nat = m2 * kLn2;
-                bool under = false;
-                if (rv) {
-                    p.lse[grow] = (use_bound ? b_nat : m_nat) + logf(l);
-                    if (p.rowmax) p.rowmax[grow] = use_bound ? __int_as_float(0x7fc00000) : m_nat;
-                    under = use_bound ? !(l >= kFltMin) : (p.bound != nullptr && b_nat - m_nat >= kUnderflowGap);
+                if (hf == 0) {
+                    const float m_nat = m2 * kLn2;
+                    bool under = false;
+                    if (rv) {
+                        p.lse[grow] = (use_bound ? b_nat : m_nat) + logf(l_row);
+                        if (p.rowmax) p.rowmax[grow] = use_bound ? __int_as_float(0x7fc00000) : m_nat;
+                        under = use_bound ? !(l_row >= kFltMin)
+                                          : (p.bound != nullptr && b_nat - m_nat >= kUnderflowGap);
+                    }
+                    const unsigned ub = __ballot_sync(0xffffffffu, under);
+                    if (p.stats && lane == 0 && ub)
+                        atomicAdd(reinterpret_cast<unsigned long long*>(&p.stats->underflow_rows),
+                                  static_cast<unsigned long long>(__popc(ub)));
                 }
-                const unsigned ub = __ballot_sync(0xffffffffu, under);
-                if (p.stats && lane == 0 && ub)
-                    atomicAdd(reinterpret_cast<unsigned long long*>(&p.stats->underflow_rows),
-                              static_cast<unsigned long long>(__popc(ub)));
             }
         }
     }
@@ -374,7 +500,7 @@ __global__ void __launch_bounds__(320, 1)
     // ------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == kWarpMma) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
@@ -414,17 +540,18 @@ static int launch_attn(const AttnLaunch& L)
         attr_done = true;
     }
     const dim3 grid(static_cast<unsigned>(L.params.n_items) * static_cast<unsigned>(L.H));
-    kern<<<grid, 320, C::SMEM_BYTES, L.stream>>>(*L.tmQ, *L.tmK, *L.tmV, L.params);
+    kern<<<grid, kAttnThreads, C::SMEM_BYTES, L.stream>>>(*L.tmK, *L.tmV, L.params);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
+
+#define FSA_FOR_EACH_TILE(X) \
+    X(64, 16) X(64, 32) X(64, 48) X(64, 64) X(128, 16) X(128, 32) X(128, 48) X(128, 64)
 
 int attn_smem_bytes(int D, int NK)
 {
 #define FSA_SMEM_CASE(d, nk) \
     if (D == d && NK == nk) return AttnCfg<d, nk>::SMEM_BYTES;
-    FSA_SMEM_CASE(64, 16) FSA_SMEM_CASE(64, 32) FSA_SMEM_CASE(64, 48) FSA_SMEM_CASE(64, 64)
-    FSA_SMEM_CASE(64, 80) FSA_SMEM_CASE(64, 96) FSA_SMEM_CASE(64, 112) FSA_SMEM_CASE(64, 128)
-    FSA_SMEM_CASE(128, 16) FSA_SMEM_CASE(128, 32) FSA_SMEM_CASE(128, 48) FSA_SMEM_CASE(128, 64) FSA_SMEM_CASE(128, 80)
+    FSA_FOR_EACH_TILE(FSA_SMEM_CASE)
 #undef FSA_SMEM_CASE
     return -1;
 }
@@ -433,9 +560,7 @@ int launch_attention(const AttnLaunch& L)
 {
 #define FSA_ATTN_CASE(d, nk) \
     if (L.D == d && L.NK == nk) return launch_attn<d, nk>(L);
-    FSA_ATTN_CASE(64, 16) FSA_ATTN_CASE(64, 32) FSA_ATTN_CASE(64, 48) FSA_ATTN_CASE(64, 64)
-    FSA_ATTN_CASE(64, 80) FSA_ATTN_CASE(64, 96) FSA_ATTN_CASE(64, 112) FSA_ATTN_CASE(64, 128)
-    FSA_ATTN_CASE(128, 16) FSA_ATTN_CASE(128, 32) FSA_ATTN_CASE(128, 48) FSA_ATTN_CASE(128, 64) FSA_ATTN_CASE(128, 80)
+    FSA_FOR_EACH_TILE(FSA_ATTN_CASE)
 #undef FSA_ATTN_CASE
     return -2;
 }

@@ -13,12 +13,14 @@ namespace fsa {
 // head; every run is a union of whole frames, ascending, disjoint.
 constexpr int kMaxRuns = 4;
 
-// Largest key tile the attention kernel supports for a head dim (TMEM budget: two query tiles
-// each hold S (NK fp32 columns) and P (NK/2 columns), plus two D-column accumulators).
-constexpr int kMaxKeyTile(int D) { return D == 128 ? 80 : 128; }
+// Largest key tile the attention kernel supports (for D = 64 and 128): each of the two query
+// tiles holds S and P (NK columns), Q (D/2 columns) and O (D columns) in 256 TMEM columns,
+// and a softmax thread keeps its half of a tile row in registers.
+constexpr int kMaxKeyTile(int D) { return 64; }
 constexpr int kRunStride = 1 + 2 * kMaxRuns;
 
 struct AttnParams {
+    const uint16_t* q;     // bf16 [H][N][D]
     const int32_t* items;  // [n_items][4]: query frame, first query row (token), valid rows tile 0, tile 1
     const int32_t* runs;   // [F][kRunStride]
     int n_items;
@@ -36,7 +38,6 @@ struct AttnParams {
 
 struct AttnLaunch {
     int D, NK, H;
-    const CUtensorMap* tmQ;
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
     AttnParams params;

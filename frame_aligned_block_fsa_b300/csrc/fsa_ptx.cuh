@@ -13,6 +13,19 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// One lane of a converged warp: true in exactly one lane (the same lane on every call
+// while the whole warp is active).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 // ----------------------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
 {
@@ -48,6 +61,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// Non-blocking test of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Shared state for bounded waits inside one CTA.
 struct WaitCtl {
     volatile int* abort;     // CTA-wide flag in shared memory
@@ -61,11 +88,47 @@ struct WaitCtl {
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w, int site,
                                           bool honour_abort = true)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test_wait(bar, parity)) return true;
     const long long t0 = clock64();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (honour_abort && *w.abort) return false;
+        if (clock64() - t0 > w.limit) {
+            *w.abort = 1;
+            if (w.err_word) atomicCAS(w.err_word, 0, -4 /* FSA_ERR_TIMEOUT */);
+            if (w.err_site) atomicCAS(w.err_site, 0, site);
+            return false;
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------- shared counters
+// A monotone counter in shared memory, for hand-offs whose waiter must react quickly: the
+// producer adds with release semantics, the waiter polls with acquire loads (a plain shared
+// load, far shorter than an mbarrier test).
+__device__ __forceinline__ uint32_t ld_acquire_shared(uint32_t addr)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_shared_add(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.release.cta.shared::cta.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// Wait until the counter reaches `target` (bounded like mbar_wait).  The abort flag and the
+// clock are checked once per 32 polls, so a poll is one shared load and a compare.
+__device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, const WaitCtl& w, int site)
+{
+    if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
+    const long long t0 = clock64();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
+        if (*w.abort) return false;
         if (clock64() - t0 > w.limit) {
             *w.abort = 1;
             if (w.err_word) atomicCAS(w.err_word, 0, -4 /* FSA_ERR_TIMEOUT */);
@@ -264,6 +327,35 @@ __device__ __forceinline__ float ex2(float x)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed fp32 pair arithmetic (one f32x2 instruction for two lanes of work): a * b + c and a + b,
+// each half rounded to nearest like the scalar fmaf / add.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "mov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\t"
+        "mov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\t"
+        "mov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
 }
 
 // Two fp32 -> packed bf16x2 (round to nearest even); `lo` lands in the low 16 bits.

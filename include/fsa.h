@@ -104,11 +104,13 @@ int fsa_plan_export(fsa_plan_t plan, int32_t* row_ptr, int32_t* col_idx, int64_t
 int fsa_plan_set_tau(fsa_plan_t plan, float tau);
 
 /*
- * fsa_plan_set_key_tile -- key rows per tensor-core tile: 0 = automatic (the largest
- * multiple of 16 that divides T and fits the kernel: at most 80 for D = 128, 128 for
- * D = 64), else a multiple of 16 in [16, 128] dividing T; a tile above the limit for the
- * call's D makes fsa_forward* return FSA_ERR_UNSUPPORTED.  Results are bitwise independent
- * of `block`; they may change in the last bits with the key tile (summation order).
+ * fsa_plan_set_key_tile -- keys per tensor-core tile: 0 = automatic (the kernel's largest,
+ * 64), else a multiple of 16 in [16, 128].  Every key run (a
+ * whole number of frames) is cut into tiles of this many keys and one last narrower tile
+ * of the rest (a multiple of 16, since T is); no tile is partially masked.  A tile above
+ * the limit for the call's D makes fsa_forward* return FSA_ERR_UNSUPPORTED.  Results are
+ * bitwise independent of `block`; they may change in the last bits with the key tile
+ * (summation order).
  */
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
 

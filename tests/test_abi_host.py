@@ -89,9 +89,9 @@ def test_plan_setters_validate(lib):
         for bad in (0.0, -1.0, float("nan")):
             assert lib.fsa_plan_set_tau(p.handle, bad) == fsa.FSA_ERR_INVALID_ARG
         assert lib.fsa_plan_set_tau(p.handle, 10.0) == fsa.FSA_OK
-        for bad in (8, 24, 144, 112, -16):
+        for bad in (8, 24, 136, 144, -16):
             assert lib.fsa_plan_set_key_tile(p.handle, bad) == fsa.FSA_ERR_INVALID_ARG, bad
-        for good in (0, 16, 48, 80):
+        for good in (0, 16, 48, 64, 80, 112, 128):
             assert lib.fsa_plan_set_key_tile(p.handle, good) == fsa.FSA_OK
 
 
