@@ -167,9 +167,14 @@ def cpu_oracle_leg(wl, target_seconds: float, seed_rows: int = 7):
         flops = sum(4 * wl.D * wl.T * oracle.frame_set_size(wl.F, wl.w, wl.ref, int(f)) for f in frames)
         return n, dt, flops
 
-    n0, dt0, _ = run(2 * threads)
-    n = max(threads, int(target_seconds * n0 / max(dt0, 1e-6)))
-    n, dt, flops = run(n)
+    run(threads)  # warm-up: thread start-up and first touch of the inputs
+    # batches of rows until about target_seconds of oracle time have been measured
+    n, dt, flops, batch = 0, 0.0, 0, 64 * threads
+    while dt < target_seconds:
+        bn, bdt, bfl = run(batch)
+        n, dt, flops = n + bn, dt + bdt, flops + bfl
+        if bdt < 0.25 * target_seconds:
+            batch *= 2
     return {"value": flops / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"{n} random rows of {wl.name} (all heads), fp64 dense masked attention over all "
                       f"{wl.N} keys per row, {dt:.1f} s"}
