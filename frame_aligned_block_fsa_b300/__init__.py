@@ -6,13 +6,16 @@ Public API (thin wrappers over the C ABI in include/fsa.h; every step runs in li
     norms(q, k, plan, qnorm, kmax, bound, eligible)   # fsa_norms
     out, lse = forward(q, k, v, plan, mode)    # fsa_forward, mode "norm_bound" | "online_max"
     forward_ex(...)                            # fsa_forward_ex
+    out, lse = forward_host(q, k, v, plan)     # fsa_forward_host (host tensors, overlapped copies)
 
 The library is loaded lazily on first use; importing the package needs no GPU.
 """
 from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_SCRATCH_LIMIT, FSA_ERR_TIMEOUT,  # noqa: F401
                    FSA_ERR_UNSUPPORTED, FSA_OK,
-                   FsaError, Plan, forward, forward_ex, load, new_stats, norms, norms_noalloc, read_stats,
+                   FsaError, Plan, forward, forward_ex, forward_host, load, new_stats, norms, norms_noalloc,
+                   read_stats,
                    selftest_wait_timeout, status_string)
 
-__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "new_stats", "read_stats", "selftest_wait_timeout",
+__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "forward_host", "new_stats", "read_stats",
+           "selftest_wait_timeout",
            "status_string", "load", "FsaError"]

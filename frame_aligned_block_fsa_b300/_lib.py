@@ -27,8 +27,8 @@ FSA_ERR_SCRATCH_LIMIT = -5
 
 # Exported symbols, in the order include/fsa.h declares them.
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
-           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_norms_noalloc", "fsa_status_string",
-           "fsa_selftest_wait_timeout")
+           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_norms_noalloc",
+           "fsa_status_string", "fsa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -66,6 +66,8 @@ def load():
             lib.fsa_forward.restype = i32
             lib.fsa_forward_ex.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp, vp, vp, vp]
             lib.fsa_forward_ex.restype = i32
+            lib.fsa_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, vp]
+            lib.fsa_forward_host.restype = i32
             lib.fsa_norms_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.fsa_norms_noalloc.restype = i32
             lib.fsa_status_string.argtypes = [i32]
@@ -199,6 +201,37 @@ def forward(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=None, s
     st = _stream_handle(stream)
     _check("fsa_forward", load().fsa_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), H, D,
                                              plan.handle, MODES[mode], st))
+    return out, lse
+
+
+def forward_host(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=None, heads_per_chunk: int = 0,
+                 stream=None):
+    """fsa_forward_host: q, k, v are host (CPU) bf16 [H, N, D] tensors, pinned for overlap.
+
+    Returns host (out fp32 [H,N,D], lse fp32 [H,N]); they are complete once `stream` (the
+    current CUDA stream by default) has been synchronised.
+    """
+    import torch
+
+    q0 = q
+    if q0.dim() != 3:
+        raise ValueError("expected [H, N, D] tensors")
+    H, N, D = q0.shape
+    if N != plan.N:
+        raise ValueError(f"sequence length {N} != plan F*T = {plan.N}")
+    for t in (q, k, v):
+        if t.shape != q0.shape or t.dtype != torch.bfloat16 or t.is_cuda or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous host bf16 tensors of one shape [H, N, D]")
+    pin = q0.is_pinned()
+    if out is None:
+        out = torch.empty((H, N, D), dtype=torch.float32, pin_memory=pin)
+    if lse is None:
+        lse = torch.empty((H, N), dtype=torch.float32, pin_memory=pin)
+    if out.is_cuda or lse.is_cuda or out.dtype != torch.float32 or lse.dtype != torch.float32:
+        raise ValueError("out and lse must be host fp32 tensors")
+    st = _stream_handle(stream)
+    _check("fsa_forward_host", load().fsa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), H, D,
+                                                       plan.handle, MODES[mode], int(heads_per_chunk), st))
     return out, lse
 
 

@@ -41,6 +41,15 @@ struct fsa_plan_s {
     float* d_ksum = nullptr;
     unsigned* d_gmax = nullptr;
     uint8_t* d_elig = nullptr;
+    // fsa_forward_host: device copies of the problem, three streams and per-chunk events
+    int64_t cap_in = 0, cap_out = 0, cap_lse = 0;  // elements
+    uint16_t* d_hq = nullptr;
+    uint16_t* d_hk = nullptr;
+    uint16_t* d_hv = nullptr;
+    float* d_hout = nullptr;
+    float* d_hlse = nullptr;
+    cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
+    std::vector<cudaEvent_t> ev;                     // [2 * chunks + 1]
 };
 
 namespace {
@@ -176,6 +185,78 @@ int run_norms(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, int H, int D,
     L.stream = stream;
     const int rc = fsa::launch_norms(L);
     return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}
+
+// The attention step on device tensors; the caller holds the plan lock and has checked the
+// arguments.  Runs the norms into the plan workspace first when norm_bound has no bound.
+int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse,
+                   int H, int D, int NK, int mode, const float* bound, const uint8_t* eligible, float* rowmax,
+                   fsa_stats_t* dev_stats, cudaStream_t st)
+{
+    int rc;
+    if (mode == FSA_MODE_NORM_BOUND && bound == nullptr) {
+        if ((rc = ensure_workspace(P, H, D)) != FSA_OK) return rc;
+        if ((rc = run_norms(P, q, k, H, D, nullptr, nullptr, nullptr, nullptr, st)) != FSA_OK) return rc;
+        bound = P->d_bound;
+        eligible = P->d_elig;
+    }
+    const int64_t rows = static_cast<int64_t>(H) * P->N;
+    CUtensorMap mk, mv;
+    if ((rc = make_tensor_map(&mk, k, rows, D, NK)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
+    fsa::AttnLaunch L;
+    L.D = D;
+    L.NK = NK;
+    L.H = H;
+    L.tmK = &mk;
+    L.tmV = &mv;
+    L.stream = st;
+    L.params.q = q;
+    L.params.items = P->d_items;
+    L.params.runs = P->d_runs;
+    L.params.n_items = P->n_items;
+    L.params.N = static_cast<int>(P->N);
+    L.params.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    L.params.mode = mode;
+    L.params.bound = bound;
+    L.params.eligible = eligible;
+    L.params.out = out;
+    L.params.lse = lse;
+    L.params.rowmax = rowmax;
+    L.params.stats = dev_stats;
+    L.params.wait_limit = kDefaultWaitLimit;
+    rc = fsa::launch_attention(L);
+    return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}
+
+// Device copies of a host problem, streams and events for fsa_forward_host.
+int ensure_host_pipeline(fsa_plan_s* P, int H, int D, int chunks)
+{
+    const int64_t in = static_cast<int64_t>(H) * P->N * D;
+    const int64_t hn = static_cast<int64_t>(H) * P->N;
+    int rc;
+    if (P->cap_in < in) {
+        cudaFree(P->d_hq);
+        cudaFree(P->d_hk);
+        cudaFree(P->d_hv);
+        P->d_hq = P->d_hk = P->d_hv = nullptr;
+        P->cap_in = 0;
+        if (cudaMalloc(reinterpret_cast<void**>(&P->d_hq), in * 2) != cudaSuccess ||
+            cudaMalloc(reinterpret_cast<void**>(&P->d_hk), in * 2) != cudaSuccess ||
+            cudaMalloc(reinterpret_cast<void**>(&P->d_hv), in * 2) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        P->cap_in = in;
+    }
+    if ((rc = grow(&P->d_hout, &P->cap_out, in)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_hlse, &P->cap_lse, hn)) != FSA_OK) return rc;
+    for (cudaStream_t* s : {&P->s_in, &P->s_comp, &P->s_out})
+        if (!*s && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) != cudaSuccess) return FSA_ERR_CUDA;
+    while (static_cast<int>(P->ev.size()) < 2 * chunks + 1) {
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return FSA_ERR_CUDA;
+        P->ev.push_back(e);
+    }
+    return FSA_OK;
 }
 
 }  // namespace
@@ -330,6 +411,14 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_ksum);
         cudaFree(plan->d_gmax);
         cudaFree(plan->d_elig);
+        cudaFree(plan->d_hq);
+        cudaFree(plan->d_hk);
+        cudaFree(plan->d_hv);
+        cudaFree(plan->d_hout);
+        cudaFree(plan->d_hlse);
+        for (cudaStream_t s : {plan->s_in, plan->s_comp, plan->s_out})
+            if (s) cudaStreamDestroy(s);
+        for (cudaEvent_t e : plan->ev) cudaEventDestroy(e);
         if (cur >= 0) cudaSetDevice(cur);
     }
     delete plan;
@@ -391,45 +480,75 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
     std::lock_guard<std::mutex> lock(plan->mu);
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
     if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
-    if (mode == FSA_MODE_NORM_BOUND && bound == nullptr) {
-        if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
-        if ((rc = run_norms(plan, q, k, H, D, nullptr, nullptr, nullptr, nullptr, st)) != FSA_OK) return rc;
-        bound = plan->d_bound;
-        eligible = plan->d_elig;
-    }
-    const int64_t rows = static_cast<int64_t>(H) * plan->N;
-    CUtensorMap mk, mv;
-    if ((rc = make_tensor_map(&mk, k, rows, D, NK)) != FSA_OK) return rc;
-    if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
-    fsa::AttnLaunch L;
-    L.D = D;
-    L.NK = NK;
-    L.H = H;
-    L.tmK = &mk;
-    L.tmV = &mv;
-    L.stream = st;
-    L.params.q = q;
-    L.params.items = plan->d_items;
-    L.params.runs = plan->d_runs;
-    L.params.n_items = plan->n_items;
-    L.params.N = static_cast<int>(plan->N);
-    L.params.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    L.params.mode = mode;
-    L.params.bound = bound;
-    L.params.eligible = eligible;
-    L.params.out = out;
-    L.params.lse = lse;
-    L.params.rowmax = rowmax;
-    L.params.stats = dev_stats;
-    L.params.wait_limit = kDefaultWaitLimit;
-    rc = fsa::launch_attention(L);
-    return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+    return forward_locked(plan, q, k, v, out, lse, H, D, NK, mode, bound, eligible, rowmax, dev_stats, st);
 }
 
 int fsa_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,
                 fsa_plan_t plan, int mode, void* stream)
 {
     return fsa_forward_ex(q, k, v, out, lse, H, D, plan, mode, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,
+                     fsa_plan_t plan, int mode, int heads_per_chunk, void* stream)
+{
+    int rc = check_shape(plan, H, D);
+    if (rc != FSA_OK) return rc;
+    if (mode != FSA_MODE_NORM_BOUND && mode != FSA_MODE_ONLINE_MAX) return FSA_ERR_INVALID_ARG;
+    if (heads_per_chunk < 0) return FSA_ERR_INVALID_ARG;
+    if (H == 0) return FSA_OK;
+    if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
+    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile(D);
+    if (NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
+    const int hc = heads_per_chunk ? std::min(heads_per_chunk, H) : std::max(1, (H + 7) / 8);
+    const int chunks = (H + hc - 1) / hc;
+    cudaStream_t caller = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if ((rc = ensure_device(plan)) != FSA_OK) return rc;
+    if ((rc = ensure_host_pipeline(plan, H, D, chunks)) != FSA_OK) return rc;
+    if (mode == FSA_MODE_NORM_BOUND && (rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
+    fsa_plan_s* P = plan;
+    const int64_t per_head = P->N * D;  // elements of one head's q, k, v or out
+    cudaEvent_t start = P->ev[2 * chunks];
+    // the pipeline starts after the work already on the caller's stream
+    if (cudaEventRecord(start, caller) != cudaSuccess || cudaStreamWaitEvent(P->s_in, start, 0) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    for (int c = 0; c < chunks; ++c) {
+        const int h0 = c * hc;
+        const int nh = std::min(hc, H - h0);
+        const int64_t off = h0 * per_head;
+        const size_t in_bytes = static_cast<size_t>(nh) * per_head * 2;
+        cudaEvent_t landed = P->ev[2 * c], done = P->ev[2 * c + 1];
+        if (cudaMemcpyAsync(P->d_hq + off, q + off, in_bytes, cudaMemcpyHostToDevice, P->s_in) != cudaSuccess ||
+            cudaMemcpyAsync(P->d_hk + off, k + off, in_bytes, cudaMemcpyHostToDevice, P->s_in) != cudaSuccess ||
+            cudaMemcpyAsync(P->d_hv + off, v + off, in_bytes, cudaMemcpyHostToDevice, P->s_in) != cudaSuccess ||
+            cudaEventRecord(landed, P->s_in) != cudaSuccess || cudaStreamWaitEvent(P->s_comp, landed, 0) != cudaSuccess)
+            return FSA_ERR_CUDA;
+        const float* bnd = nullptr;
+        const uint8_t* elg = nullptr;
+        if (mode == FSA_MODE_NORM_BOUND) {
+            float* b = P->d_bound + h0 * P->N;
+            uint8_t* e = P->d_elig + h0;
+            if ((rc = run_norms(P, P->d_hq + off, P->d_hk + off, nh, D, nullptr, nullptr, b, e, P->s_comp)) != FSA_OK)
+                return rc;
+            bnd = b;
+            elg = e;
+        }
+        if ((rc = forward_locked(P, P->d_hq + off, P->d_hk + off, P->d_hv + off, P->d_hout + off,
+                                 P->d_hlse + h0 * P->N, nh, D, NK, mode, bnd, elg, nullptr, nullptr, P->s_comp)) !=
+            FSA_OK)
+            return rc;
+        if (cudaEventRecord(done, P->s_comp) != cudaSuccess || cudaStreamWaitEvent(P->s_out, done, 0) != cudaSuccess ||
+            cudaMemcpyAsync(out + off, P->d_hout + off, static_cast<size_t>(nh) * per_head * 4,
+                            cudaMemcpyDeviceToHost, P->s_out) != cudaSuccess ||
+            cudaMemcpyAsync(lse + h0 * P->N, P->d_hlse + h0 * P->N, static_cast<size_t>(nh) * P->N * 4,
+                            cudaMemcpyDeviceToHost, P->s_out) != cudaSuccess)
+            return FSA_ERR_CUDA;
+    }
+    // the caller's stream resumes once the last results are on the host
+    if (cudaEventRecord(start, P->s_out) != cudaSuccess || cudaStreamWaitEvent(caller, start, 0) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    return FSA_OK;
 }
 
 int fsa_selftest_wait_timeout(long long limit_cycles, int32_t* status, void* stream)

@@ -162,6 +162,31 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
                    fsa_stats_t* dev_stats, void* stream);
 
 /*
+ * fsa_forward_host -- fsa_forward on host tensors, with the copies overlapped.
+ * The pages have no counterpart (their pipeline keeps activations on the accelerator); this
+ * is the library's end-to-end entry for callers whose q, k, v live in host memory.  The
+ * heads are split into chunks of heads_per_chunk heads (0 = automatic, about eight
+ * chunks).  Chunk c is copied to the device on one stream, computed (fsa_norms in
+ * norm_bound mode, then the attention) on a second, and its out and lse are copied back on
+ * a third, so the host-to-device copy of chunk c+1, the compute of chunk c and the
+ * device-to-host copy of chunk c-1 run at the same time.  Heads are independent, so the
+ * results equal those of fsa_forward on device copies of the same tensors, bit for bit.
+ *   q, k, v: host bf16 [H][N][D]; out: host fp32 [H][N][D]; lse: host fp32 [H][N].  Page-locked
+ *   (pinned) host memory is needed for the copies to overlap; pageable memory works but
+ *   serialises them.
+ *   The pipeline starts after the work already queued on `stream` and `stream` waits for its
+ *   end: synchronise `stream` before reading out and lse.  The host buffers must stay valid
+ *   and unchanged until then.
+ *   The plan keeps device copies of the whole problem (3 x H*N*D bf16 + H*N*D and H*N fp32),
+ *   three streams and the events, grown on the first call for a given size (cudaMalloc: make
+ *   that call before any stream capture) and freed by fsa_plan_destroy.
+ * Errors as fsa_forward, plus FSA_ERR_INVALID_ARG for heads_per_chunk < 0.  A CUDA error in
+ * the middle returns FSA_ERR_CUDA with earlier chunks possibly still in flight.
+ */
+int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse,
+                     int H, int D, fsa_plan_t plan, int mode, int heads_per_chunk, void* stream);
+
+/*
  * fsa_norms_noalloc -- fsa_norms for callers that cannot allocate device memory.
  * The pages have no counterpart; this is a service of the library.  fsa_norms keeps its
  * scratch (per-frame key sums, per-head maxima) in a plan workspace grown with cudaMalloc,

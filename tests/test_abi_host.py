@@ -120,6 +120,17 @@ def test_forward_rejects_bad_arguments_before_device_work(lib):
         assert lib.fsa_norms(fake, fake, 0, 64, h, None, None, None, None, None) == fsa.FSA_OK
         assert ex(*args(H=0, q=None, k=None, v=None, out=None, lse=None)) == fsa.FSA_OK
         assert lib.fsa_forward(fake, fake, fake, fake, fake, 2, 64, h, 7, None) == fsa.FSA_ERR_INVALID_ARG
+        fh = lib.fsa_forward_host
+        hargs = lambda **kw: [kw.get("q", fake), kw.get("k", fake), kw.get("v", fake), kw.get("out", fake),
+                              kw.get("lse", fake), kw.get("H", 2), kw.get("D", 64), kw.get("plan", h),
+                              kw.get("mode", 0), kw.get("hpc", 0), None]
+        assert fh(*hargs(D=96)) == fsa.FSA_ERR_UNSUPPORTED
+        assert fh(*hargs(mode=3)) == fsa.FSA_ERR_INVALID_ARG
+        assert fh(*hargs(hpc=-1)) == fsa.FSA_ERR_INVALID_ARG
+        assert fh(*hargs(v=None)) == fsa.FSA_ERR_INVALID_ARG
+        assert fh(*hargs(out=None)) == fsa.FSA_ERR_INVALID_ARG
+        assert fh(*hargs(plan=None)) == fsa.FSA_ERR_INVALID_ARG
+        assert fh(*hargs(H=0)) == fsa.FSA_OK
     # a key tile above the kernel's TMEM budget for D = 128 is refused before device work
     with fsa.Plan(4, 256, 1, 0, 64) as p:
         p.set_key_tile(128)

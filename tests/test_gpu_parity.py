@@ -220,6 +220,26 @@ def test_head_group_invariance_bitwise(dev, mode):
     assert torch.equal(full["lse_t"].cpu(), torch.cat([a["lse_t"].cpu(), b["lse_t"].cpu()]))
 
 
+@pytest.mark.parametrize("mode", ["norm_bound", "online_max"])
+@pytest.mark.parametrize("heads_per_chunk,pinned", [(0, True), (3, True), (1, True), (8, False)])
+def test_forward_host_equals_device_bitwise(dev, mode, heads_per_chunk, pinned):
+    # host tensors in, chunks of heads pipelined over three streams: same bits as the device
+    # call (heads are independent); 3 heads per chunk leaves a ragged last chunk of 2
+    wl = WORKLOADS["small"]
+    q, k, v = _inputs("small")
+    v2 = (v.float() * -0.5).to(torch.bfloat16)
+    refs = [_gpu(dev, q, k, vv, wl.F, wl.T, wl.w, wl.ref, wl.block, mode) for vv in (v, v2)]
+    if pinned:
+        q, k, v, v2 = q.pin_memory(), k.pin_memory(), v.pin_memory(), v2.pin_memory()
+    with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+        for vv, ref in zip((v, v2), refs):  # the second call reuses the plan's device copies
+            out, lse = fsa.forward_host(q, k, vv, plan, mode, heads_per_chunk=heads_per_chunk)
+            torch.cuda.current_stream().synchronize()
+            assert not out.is_cuda and out.is_pinned() == pinned
+            assert torch.equal(out, ref["out_t"].cpu())
+            assert torch.equal(lse, ref["lse_t"].cpu())
+
+
 def test_forced_fallback_equals_online_bitwise(dev):
     wl = WORKLOADS["small"]
     q, k, v = _inputs("small")
