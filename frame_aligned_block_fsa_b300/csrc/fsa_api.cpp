@@ -35,6 +35,11 @@ struct fsa_plan_s {
     int32_t* d_items = nullptr;
     // norms workspace, grown on demand (capacities in elements)
     int64_t cap_qnorm = 0, cap_bound = 0, cap_kmax = 0, cap_ksum = 0, cap_gmax = 0, cap_elig = 0;
+    int64_t cap_psum = 0, cap_pmax = 0, cap_tickets = 0;
+    float* d_psum = nullptr;
+    float* d_pmax = nullptr;
+    unsigned* d_tickets = nullptr;
+    bool tickets_fresh = false;  // newly allocated: zero them on the next norms launch
     float* d_qnorm = nullptr;
     float* d_bound = nullptr;
     float* d_kmax = nullptr;
@@ -121,6 +126,12 @@ int ensure_workspace(fsa_plan_s* P, int H, int D)
     if ((rc = grow(&P->d_kmax, &P->cap_kmax, hf)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_ksum, &P->cap_ksum, hf * D)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_gmax, &P->cap_gmax, static_cast<int64_t>(H))) != FSA_OK) return rc;
+    const int64_t chunks = fsa::norms_key_chunks(P->T);
+    if ((rc = grow(&P->d_psum, &P->cap_psum, hf * chunks * D)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_pmax, &P->cap_pmax, hf * chunks)) != FSA_OK) return rc;
+    const int64_t had = P->cap_tickets;
+    if ((rc = grow(&P->d_tickets, &P->cap_tickets, hf)) != FSA_OK) return rc;
+    if (P->cap_tickets != had) P->tickets_fresh = true;
     return grow(&P->d_elig, &P->cap_elig, static_cast<int64_t>(H));
 }
 
@@ -179,6 +190,15 @@ int run_norms(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, int H, int D,
     L.qnorm = qnorm;
     L.kmax = kmax ? kmax : P->d_kmax;
     L.ksum = P->d_ksum;
+    L.part_sum = P->d_psum;
+    L.part_max = P->d_pmax;
+    L.tickets = P->d_tickets;
+    if (P->tickets_fresh) {
+        if (cudaMemsetAsync(P->d_tickets, 0, static_cast<size_t>(P->cap_tickets) * sizeof(unsigned), stream) !=
+            cudaSuccess)
+            return FSA_ERR_CUDA;
+        P->tickets_fresh = false;
+    }
     L.bound = bound ? bound : P->d_bound;
     L.gmax = P->d_gmax;
     L.eligible = eligible ? eligible : P->d_elig;
@@ -410,6 +430,9 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_kmax);
         cudaFree(plan->d_ksum);
         cudaFree(plan->d_gmax);
+        cudaFree(plan->d_psum);
+        cudaFree(plan->d_pmax);
+        cudaFree(plan->d_tickets);
         cudaFree(plan->d_elig);
         cudaFree(plan->d_hq);
         cudaFree(plan->d_hk);

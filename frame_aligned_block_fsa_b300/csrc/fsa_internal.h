@@ -58,6 +58,9 @@ struct NormsLaunch {
     float* qnorm;          // [H][N] or null
     float* kmax;           // [H][F]
     float* ksum;           // [H][F][D] workspace
+    float* part_sum;       // [H][F][chunks][D] workspace: column sums of a chunk of a frame's keys
+    float* part_max;       // [H][F][chunks] workspace: the chunk's max key norm
+    unsigned* tickets;     // [H][F] workspace, zero between launches (each launch leaves it zero)
     float* bound;          // [H][N]
     unsigned* gmax;        // [H] workspace
     uint8_t* eligible;     // [H]
@@ -65,6 +68,9 @@ struct NormsLaunch {
 };
 
 int launch_norms(const NormsLaunch& L);
+// Chunks of a frame's keys that key_frame_stats reads in separate blocks (1..kMaxKeyChunks).
+constexpr int kMaxKeyChunks = 8;
+int norms_key_chunks(int T);
 
 // Read-only view of a plan's host data, for entry points that live outside fsa_api.cpp.
 struct PlanView {

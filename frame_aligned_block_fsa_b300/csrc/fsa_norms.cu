@@ -6,9 +6,12 @@
 // it starts.  The bound is taken over each row's own key set (the window frames and the
 // reference frame), which is what makes it valid for the windowed mask.
 //
-// Three HBM-bound kernels (bf16 rows read with 128-bit loads, 16 threads per 256-byte row):
-//   1. key_frame_stats   one block per (frame, head): max key norm of the frame and the
-//                        per-frame column sums of K (for the mean key of a key set);
+// Three HBM-bound kernels (bf16 rows read with 128-bit loads, D/16 threads per row, packed
+// f32x2 arithmetic):
+//   1. key_frame_stats   per (chunk of a frame's rows, frame, head): the chunk's max key norm
+//                        and column sums of K; the last chunk of a frame to finish reduces
+//                        the chunks in a fixed order into the frame's max key norm and key
+//                        sums (a ticket counter, no waiting);
 //   2. query_bounds      per (row chunk, frame, head): ||q||, bound = c ||q|| Kmax_S, and the
 //                        gap bound c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head;
 //   3. eligibility       per head: max gap bound <= tau.
@@ -49,67 +52,168 @@ __device__ __forceinline__ float group_sum(float v)
     return v;
 }
 
+constexpr int kNormThreads = 256;
+constexpr int kBatch = 2;  // row iterations whose loads are issued together (2 x 2 x 16 B per thread)
+
+// A thread reads 16 bf16 of a row as two 16-byte loads, D/2 columns apart, so that the row's
+// D/16 threads cover a contiguous half-row with each load.  Its columns are
+// [8 sub, 8 sub + 8) and [D/2 + 8 sub, D/2 + 8 sub + 8).
 template <int D>
-__global__ void __launch_bounds__(256) key_frame_stats_kernel(const uint16_t* __restrict__ k, int N, int T,
-                                                              int F, float* __restrict__ kmax,
-                                                              float* __restrict__ ksum,
-                                                              unsigned* __restrict__ gmax)
+__device__ __forceinline__ void load_row16(const uint4* row, int sub, bool act, uint4& a, uint4& b)
 {
-    constexpr int TPR = D / 8;       // threads per row, 16 bytes each
-    constexpr int RPI = 256 / TPR;   // rows per block iteration
+    if (act) {
+        a = ldg_stream(row + sub);
+        b = ldg_stream(row + D / 16 + sub);
+    } else {
+        a = make_uint4(0u, 0u, 0u, 0u);
+        b = a;
+    }
+}
+
+// The 16 values of a thread as 8 pairs (x[2i], x[2i+1]).
+__device__ __forceinline__ void unpack16(const uint4& a, const uint4& b, float2* x)
+{
+    const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b)
+{
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) key_frame_stats_kernel(
+    const uint16_t* __restrict__ k, int N, int T, int F, int chunks, int rows_per_chunk,
+    float* __restrict__ part_max, float* __restrict__ part_sum, unsigned* __restrict__ tickets,
+    float* __restrict__ kmax, float* __restrict__ ksum, unsigned* __restrict__ gmax)
+{
+    constexpr int TPR = D / 16;                // threads per row, 16 values each
+    constexpr int RPI = kNormThreads / TPR;    // rows per block iteration
     __shared__ float cs[RPI][D + 1];
-    __shared__ float wmax[8];
-    const int g = blockIdx.x, h = blockIdx.y;
+    __shared__ float wmax[kNormThreads / 32];
+    __shared__ bool last;
+    const int c = blockIdx.x, g = blockIdx.y, h = blockIdx.z;
     const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
+    const int r0 = c * rows_per_chunk;
+    const int r1 = min(T, r0 + rows_per_chunk);
     const uint4* base = reinterpret_cast<const uint4*>(k + (static_cast<int64_t>(h) * N + static_cast<int64_t>(g) * T) * D);
-    float csum[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    float2 csum[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) csum[i] = make_float2(0.0f, 0.0f);
     float mx = 0.0f;
     // the trip count is uniform across the block so the row-group shuffles stay converged
-#pragma unroll 4
-    for (int rb = 0; rb < T; rb += RPI) {
-        const int r = rb + rsel;
-        float x[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (r < T) unpack8(ldg_stream(base + static_cast<int64_t>(r) * TPR + sub), x);
-        float ss = 0.0f;
+    for (int rb = r0; rb < r1; rb += kBatch * RPI) {
+        uint4 ua[kBatch], ub[kBatch];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            ss = fmaf(x[e], x[e], ss);
-            csum[e] += x[e];
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = rb + b * RPI + rsel;
+            load_row16<D>(base + static_cast<int64_t>(r) * (D / 8), sub, r < r1, ua[b], ub[b]);
         }
-        ss = group_sum<TPR>(ss);
-        mx = fmaxf(mx, sqrtf(ss));
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            float2 x[8];
+            unpack16(ua[b], ub[b], x);
+            float2 ss = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ss = fma2(x[i], x[i], ss);
+                csum[i] = add2(csum[i], x[i]);
+            }
+            const float n2 = group_sum<TPR>(ss.x + ss.y);
+            mx = fmaxf(mx, sqrtf(n2));
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) cs[rsel][sub * 8 + e] = csum[e];
+    for (int i = 0; i < 8; ++i) {
+        // pair i holds columns (2i, 2i+1) of the thread's 16: the first 4 pairs lie in the
+        // first half-row, the last 4 in the second
+        const int col = (i < 4 ? 8 * sub + 2 * i : D / 2 + 8 * sub + 2 * (i - 4));
+        cs[rsel][col] = csum[i].x;
+        cs[rsel][col + 1] = csum[i].y;
+    }
     __syncthreads();
+    const int64_t hg = static_cast<int64_t>(h) * F + g;
     if (threadIdx.x < D) {
         float s = 0.0f;
         for (int r = 0; r < RPI; ++r) s += cs[r][threadIdx.x];
-        ksum[(static_cast<int64_t>(h) * F + g) * D + threadIdx.x] = s;
+        part_sum[(hg * chunks + c) * D + threadIdx.x] = s;
     }
     if (threadIdx.x == 0) {
         float m = wmax[0];
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
-        kmax[static_cast<int64_t>(h) * F + g] = m;
-        if (g == 0) gmax[h] = 0u;
+        for (int w = 1; w < kNormThreads / 32; ++w) m = fmaxf(m, wmax[w]);
+        part_max[hg * chunks + c] = m;
+        if (c == 0 && g == 0) gmax[h] = 0u;
+    }
+    // The last chunk of this frame to finish reduces all chunks, in chunk order.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned ticket = atomicAdd(tickets + hg, 1u);
+        last = ticket == static_cast<unsigned>(chunks - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (threadIdx.x < D) {
+        float s = 0.0f;
+        for (int i = 0; i < chunks; ++i) s += __ldcg(part_sum + (hg * chunks + i) * D + threadIdx.x);
+        ksum[hg * D + threadIdx.x] = s;
+    }
+    if (threadIdx.x == 0) {
+        float m = 0.0f;
+        for (int i = 0; i < chunks; ++i) m = fmaxf(m, __ldcg(part_max + hg * chunks + i));
+        kmax[hg] = m;
+        tickets[hg] = 0u;  // ready for the next launch
     }
 }
 
 template <int D>
-__global__ void __launch_bounds__(256) query_bounds_kernel(
+__global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
     const uint16_t* __restrict__ q, int N, int T, int F, const int32_t* __restrict__ runs, float scale,
     const float* __restrict__ kmax, const float* __restrict__ ksum, float* __restrict__ qnorm,
     float* __restrict__ bound, unsigned* __restrict__ gmax, int rows_per_block)
 {
-    constexpr int TPR = D / 8;
-    constexpr int RPI = 256 / TPR;
+    constexpr int TPR = D / 16;
+    constexpr int RPI = kNormThreads / TPR;
     __shared__ float kbar[D];
     __shared__ float kh_s;
-    __shared__ float wmax[8];
+    __shared__ float wmax[kNormThreads / 32];
     const int f = blockIdx.y, h = blockIdx.z;
+    const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
+    const int r0 = blockIdx.x * rows_per_block;
+    const int r1 = min(T, r0 + rows_per_block);
+    const int64_t row_base = static_cast<int64_t>(h) * N + static_cast<int64_t>(f) * T;
+    const uint4* base = reinterpret_cast<const uint4*>(q + row_base * D);
+    // The first batch of query rows is in flight while the key statistics of the row's key
+    // set are gathered from L2.
+    uint4 ua[kBatch], ub[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+        const int r = r0 + b * RPI + rsel;
+        load_row16<D>(base + static_cast<int64_t>(r) * (D / 8), sub, r < r1, ua[b], ub[b]);
+    }
     const int32_t* rr = runs + f * kRunStride;
     const int n_runs = rr[0];
     if (threadIdx.x < D) {
@@ -117,50 +221,62 @@ __global__ void __launch_bounds__(256) query_bounds_kernel(
         int count = 0;
         for (int r = 0; r < n_runs; ++r) {
             const int g0 = rr[1 + 2 * r] / T, ng = rr[2 + 2 * r] / T;
-            for (int g = g0; g < g0 + ng; ++g) s += ksum[(static_cast<int64_t>(h) * F + g) * D + threadIdx.x];
+            const float* src = ksum + (static_cast<int64_t>(h) * F + g0) * D + threadIdx.x;
+#pragma unroll 8
+            for (int g = 0; g < ng; ++g) s += src[static_cast<int64_t>(g) * D];
             count += rr[2 + 2 * r];
         }
         kbar[threadIdx.x] = s / static_cast<float>(count);
-    }
-    if (threadIdx.x == 0) {
+    } else if (threadIdx.x < D + 32) {
+        // one warp: the largest key norm of the key set, one frame per lane
+        const int lane = threadIdx.x - D;
         float m = 0.0f;
         for (int r = 0; r < n_runs; ++r) {
             const int g0 = rr[1 + 2 * r] / T, ng = rr[2 + 2 * r] / T;
-            for (int g = g0; g < g0 + ng; ++g) m = fmaxf(m, kmax[static_cast<int64_t>(h) * F + g]);
+            for (int i = lane; i < ng; i += 32) m = fmaxf(m, kmax[static_cast<int64_t>(h) * F + g0 + i]);
         }
-        kh_s = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) kh_s = m;
     }
     __syncthreads();
     const float K = kh_s;
-    const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
-    float kb[8];
+    float2 kb[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) kb[e] = kbar[sub * 8 + e];
-    const int r0 = blockIdx.x * rows_per_block;
-    const int r1 = min(T, r0 + rows_per_block);
-    const int64_t row_base = static_cast<int64_t>(h) * N + static_cast<int64_t>(f) * T;
-    const uint4* base = reinterpret_cast<const uint4*>(q + row_base * D);
+    for (int i = 0; i < 8; ++i) {
+        const int col = (i < 4 ? 8 * sub + 2 * i : D / 2 + 8 * sub + 2 * (i - 4));
+        kb[i] = make_float2(kbar[col], kbar[col + 1]);
+    }
     float gworst = 0.0f;
-#pragma unroll 4
-    for (int rb = r0; rb < r1; rb += RPI) {
-        const int r = rb + rsel;
-        const bool act = r < r1;
-        float x[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if (act) unpack8(ldg_stream(base + static_cast<int64_t>(r) * TPR + sub), x);
-        float ss = 0.0f, dot = 0.0f;
+    for (int rb = r0; rb < r1; rb += kBatch * RPI) {
+        if (rb != r0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            ss = fmaf(x[e], x[e], ss);
-            dot = fmaf(x[e], kb[e], dot);
+            for (int b = 0; b < kBatch; ++b) {
+                const int r = rb + b * RPI + rsel;
+                load_row16<D>(base + static_cast<int64_t>(r) * (D / 8), sub, r < r1, ua[b], ub[b]);
+            }
         }
-        ss = group_sum<TPR>(ss);
-        dot = group_sum<TPR>(dot);
-        const float qn = sqrtf(ss);
-        const float qk = qn * K;
-        if (act) gworst = fmaxf(gworst, scale * (qk - dot));
-        if (act && sub == 0) {
-            if (qnorm) qnorm[row_base + r] = qn;
-            bound[row_base + r] = scale * qk;
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = rb + b * RPI + rsel;
+            const bool act = r < r1;
+            float2 x[8];
+            unpack16(ua[b], ub[b], x);
+            float2 ss = make_float2(0.0f, 0.0f), dot = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                ss = fma2(x[i], x[i], ss);
+                dot = fma2(x[i], kb[i], dot);
+            }
+            const float n2 = group_sum<TPR>(ss.x + ss.y);
+            const float dt = group_sum<TPR>(dot.x + dot.y);
+            const float qn = sqrtf(n2);
+            const float qk = qn * K;
+            if (act) gworst = fmaxf(gworst, scale * (qk - dt));
+            if (act && sub == 0) {
+                if (qnorm) qnorm[row_base + r] = qn;
+                bound[row_base + r] = scale * qk;
+            }
         }
     }
 #pragma unroll
@@ -169,7 +285,7 @@ __global__ void __launch_bounds__(256) query_bounds_kernel(
     __syncthreads();
     if (threadIdx.x == 0) {
         float m = wmax[0];
-        for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
+        for (int w = 1; w < kNormThreads / 32; ++w) m = fmaxf(m, wmax[w]);
         // non-negative floats order like their bit patterns
         atomicMax(gmax + h, __float_as_uint(fmaxf(m, 0.0f)));
     }
@@ -182,14 +298,25 @@ __global__ void eligibility_kernel(const unsigned* __restrict__ gmax, float tau,
     if (h < H) eligible[h] = static_cast<uint8_t>(__uint_as_float(gmax[h]) <= tau);
 }
 
+int norms_key_chunks(int T)
+{
+    const int c = T / 256;  // about 256-300 rows per block at the workload sizes
+    return c < 1 ? 1 : (c > kMaxKeyChunks ? kMaxKeyChunks : c);
+}
+
 template <int D>
 static int launch_norms_d(const NormsLaunch& L)
 {
-    key_frame_stats_kernel<D><<<dim3(L.F, L.H), 256, 0, L.stream>>>(L.k, L.N, L.T, L.F, L.kmax, L.ksum, L.gmax);
-    const int rows_per_block = 128;
-    const dim3 grid((L.T + rows_per_block - 1) / rows_per_block, L.F, L.H);
-    query_bounds_kernel<D><<<grid, 256, 0, L.stream>>>(L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum,
-                                                       L.qnorm, L.bound, L.gmax, rows_per_block);
+    const int chunks = norms_key_chunks(L.T);
+    const int rows_per_chunk = (L.T + chunks - 1) / chunks;
+    key_frame_stats_kernel<D><<<dim3(chunks, L.F, L.H), kNormThreads, 0, L.stream>>>(
+        L.k, L.N, L.T, L.F, chunks, rows_per_chunk, L.part_max, L.part_sum, L.tickets, L.kmax, L.ksum, L.gmax);
+    // about 256 query rows per block, split evenly over a frame (T = 1200: 5 blocks of 240)
+    const int qblocks = (L.T + 255) / 256;
+    const int rows_per_block = (L.T + qblocks - 1) / qblocks;
+    const dim3 grid(qblocks, L.F, L.H);
+    query_bounds_kernel<D><<<grid, kNormThreads, 0, L.stream>>>(L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum,
+                                                                L.qnorm, L.bound, L.gmax, rows_per_block);
     eligibility_kernel<<<(L.H + 127) / 128, 128, 0, L.stream>>>(L.gmax, L.tau, L.eligible, L.H);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

@@ -68,11 +68,17 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     if (!q || !k || !kmax || !bound || !eligible) return FSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return FSA_ERR_INVALID_ARG;
 
-    // scratch layout: key runs of every query frame | per-frame key sums | per-head gap maxima
+    // scratch layout: per-frame tickets | key runs of every query frame | per-frame key sums |
+    // per-chunk key sums | per-chunk max key norms | per-head gap maxima
+    const size_t hf = static_cast<size_t>(H) * pv.F;
+    const size_t chunks = static_cast<size_t>(fsa::norms_key_chunks(pv.T));
+    const size_t tickets_bytes = hf * sizeof(unsigned);
     const size_t runs_bytes = static_cast<size_t>(pv.F) * fsa::kRunStride * sizeof(int32_t);
-    const size_t off_ksum = fsa::round256(runs_bytes);
-    const size_t ksum_bytes = static_cast<size_t>(H) * pv.F * D * sizeof(float);
-    const size_t off_gmax = off_ksum + fsa::round256(ksum_bytes);
+    const size_t off_runs = fsa::round256(tickets_bytes);
+    const size_t off_ksum = off_runs + fsa::round256(runs_bytes);
+    const size_t off_psum = off_ksum + fsa::round256(hf * D * sizeof(float));
+    const size_t off_pmax = off_psum + fsa::round256(hf * chunks * D * sizeof(float));
+    const size_t off_gmax = off_pmax + fsa::round256(hf * chunks * sizeof(float));
     const size_t total = off_gmax + fsa::round256(static_cast<size_t>(H) * sizeof(unsigned));
     if (total > fsa::kNoAllocScratchBytes) return FSA_ERR_SCRATCH_LIMIT;
 
@@ -81,9 +87,12 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     if (rc != FSA_OK) return rc;
     unsigned char* s = static_cast<unsigned char*>(base);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The previous call's contents are overwritten: the runs here, the key sums by the first
-    // kernel, and the gap maxima are zeroed by the first kernel before the second max-reduces.
-    if (cudaMemcpyAsync(s, pv.runs, runs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return FSA_ERR_CUDA;
+    // The previous call's contents are overwritten: the tickets are zeroed and the runs copied
+    // here, the key sums are written by the first kernel, and the gap maxima are zeroed by the
+    // first kernel before the second max-reduces.
+    if (cudaMemsetAsync(s, 0, tickets_bytes, st) != cudaSuccess) return FSA_ERR_CUDA;
+    if (cudaMemcpyAsync(s + off_runs, pv.runs, runs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return FSA_ERR_CUDA;
 
     fsa::NormsLaunch L;
     L.q = q;
@@ -93,12 +102,15 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     L.F = pv.F;
     L.T = pv.T;
     L.N = static_cast<int>(pv.N);
-    L.runs = reinterpret_cast<const int32_t*>(s);
+    L.runs = reinterpret_cast<const int32_t*>(s + off_runs);
     L.scale = 1.0f / sqrtf(static_cast<float>(D));
     L.tau = pv.tau;
     L.qnorm = qnorm;
     L.kmax = kmax;
     L.ksum = reinterpret_cast<float*>(s + off_ksum);
+    L.part_sum = reinterpret_cast<float*>(s + off_psum);
+    L.part_max = reinterpret_cast<float*>(s + off_pmax);
+    L.tickets = reinterpret_cast<unsigned*>(s);
     L.bound = bound;
     L.gmax = reinterpret_cast<unsigned*>(s + off_gmax);
     L.eligible = eligible;

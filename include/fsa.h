@@ -194,13 +194,15 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
  * capture, engines that hand out all device memory themselves, and loops that cannot afford
  * the device synchronisation of cudaMalloc/cudaFree need a call that allocates nothing:
  * this one keeps that scratch in a fixed 2 MiB device array compiled into the library (every
- * GPU that loads the library holds it until the process exits) and copies the plan's key runs
- * into it on every call (a small host-to-device copy on `stream`).
+ * GPU that loads the library holds it until the process exits), zeroes its counters and copies
+ * the plan's key runs into it on every call (a small memset and host-to-device copy on
+ * `stream`).
  *   Arguments and results are those of fsa_norms, except that kmax, bound and eligible are
  *   required (they are the outputs; qnorm may be NULL).
- *   Limit: F*9*4 + H*F*D*4 + H*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
- *   H=24, F=24, D=128 uses 0.3 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT before any
- *   device work.
+ *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, H*F*4 + F*9*4 + H*F*D*4 +
+ *   H*F*C*D*4 + H*F*C*4 + H*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
+ *   H=24, F=24, T=1200, D=128 uses 1.5 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT
+ *   before any device work.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *   with that device current; make that first call before any stream capture.
  *   Every call shares the one array and overwrites what the previous call left there, so

@@ -90,8 +90,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch_before_device_work():
     lib = fsa.load()
     fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
     with fsa.Plan(64, 256, 1, 0, 64) as plan:
-        # 40 heads x 64 frames x 128 x 4 bytes of key sums = 1.25 MiB: fits
-        # 80 heads x 64 frames x 128 x 4 bytes = 2.5 MiB: does not
+        # 80 heads x 64 frames x 128 x 4 bytes of per-frame key sums alone are 2.5 MiB: too large
         rc = lib.fsa_norms_noalloc(fake, fake, 80, 128, plan.handle, None, fake, fake, fake, None)
         assert rc == fsa.FSA_ERR_SCRATCH_LIMIT
         assert "scratch" in fsa.status_string(rc)
