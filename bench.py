@@ -48,6 +48,9 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the online-max comparison and gap stats")
+    ap.add_argument("--sweep", action="store_true",
+                    help="instead of the bench line: one JSON line per workload and softmax mode (attention time, "
+                         "norms time, bound-gap statistics, fallback heads, underflow rows)")
     return ap.parse_args()
 
 
@@ -56,6 +59,27 @@ def dist_info():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return rank, world, local
+
+
+def rank_seed(wl, rank: int) -> int:
+    """Seed of a rank's inputs: every rank gets its own independent batch of the workload."""
+    return wl.seed + 1000 * rank
+
+
+def max_over_ranks(value: float, pg, device) -> float:
+    """The largest of the ranks' values (the whole job ends when its slowest rank does)."""
+    if pg is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, world: int, steps: int, ms: float) -> float:
+    """Whole-job TFLOP/s: the active FLOPs of every rank's steps over the slowest rank's time."""
+    return flops_per_rank_step * world * steps / (ms * 1e-3) / 1e12
 
 
 def load_peaks():
@@ -222,6 +246,71 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def sweep(args):
+    """Every workload in both softmax modes, one JSON line each (not the bench contract line)."""
+    import torch
+
+    import frame_aligned_block_fsa_b300 as fsa
+    from frame_aligned_block_fsa_b300.inputs import make_workload_inputs
+    from frame_aligned_block_fsa_b300.workloads import WORKLOADS
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, _ = load_peaks()
+    for name in ("tiny", "small", "sr28k", "sr57k", "stress"):
+        wl = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_workload_inputs(wl))
+        H, N, D = wl.H, wl.N, wl.D
+        out = torch.empty((H, N, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((H, N), dtype=torch.float32, device=dev)
+        bound = torch.empty((H, N), dtype=torch.float32, device=dev)
+        elig = torch.empty(H, dtype=torch.uint8, device=dev)
+        rm = torch.empty((H, N), dtype=torch.float32, device=dev)
+        plan = fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
+        flops = plan.nnz() * 4 * wl.block * wl.block * D * H
+        reps = max(3, min(args.steps, 20))
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(stream)
+            for _ in range(reps):
+                fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            return a.elapsed_time(b) / reps
+
+        norms_ms = timed(lambda: fsa.norms(q, k, plan, None, None, bound, elig, stream=stream))
+        # the row max comes from a running-max pass over every head
+        fsa.forward_ex(q, k, v, plan, "online_max", out=out, lse=lse, bound=bound, eligible=elig, rowmax=rm)
+        torch.cuda.synchronize()
+        gap = (bound - rm).flatten()
+        qs = torch.quantile(gap[torch.randperm(gap.numel(), device=dev)[:1 << 20]],
+                            torch.tensor([0.5, 0.99], device=dev))
+        for mode in ("norm_bound", "online_max"):
+            st = fsa.new_stats(dev)
+            fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound, eligible=elig, stats=st)
+            torch.cuda.synchronize()
+            stats = fsa.read_stats(st)
+            ms = timed(lambda: fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound, eligible=elig,
+                                              stream=stream))
+            line = {"sweep": name, "mode": mode, "workload": workload_desc(wl), "attention_ms": ms,
+                    "attention_tflops": flops / (ms * 1e-3) / 1e12,
+                    "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]),
+                    "norms_ms": norms_ms, "active_flops": flops, "eligible_heads": int(elig.sum().item()),
+                    "heads": H, "fallback_heads": stats["fallback_heads"], "underflow_rows": stats["underflow_rows"],
+                    "error": stats["error"],
+                    "bound_gap_nats": {"min": float(gap.min()), "median": float(qs[0]), "p99": float(qs[1]),
+                                       "max": float(gap.max())}}
+            print(json.dumps(line), flush=True)
+        plan.close()
+        del q, k, v, out, lse, bound, elig, rm
+        torch.cuda.empty_cache()
+
+
 def workload_desc(wl):
     return (f"{wl.name}: F={wl.F} x T={wl.T} (N={wl.N}), H={wl.H}, D={wl.D}, window +-{wl.w} + ref frame "
             f"{wl.ref}, block {wl.block}, inputs {wl.kind}, seed {wl.seed}")
@@ -232,6 +321,8 @@ def main():
     rank, world, local = dist_info()
     if args.impl == "reference":
         return reference_arm(args, rank)
+    if args.sweep:
+        return sweep(args) if rank == 0 else None
 
     import numpy as np
     import torch
@@ -253,7 +344,7 @@ def main():
     wl = WORKLOADS[args.workload]
     H, N, D = wl.H, wl.N, wl.D
     # each rank: its own independent batch of the same shape
-    q_h, k_h, v_h = make_qkv(H, N, D, seed=wl.seed + 1000 * rank, kind=wl.kind)
+    q_h, k_h, v_h = make_qkv(H, N, D, seed=rank_seed(wl, rank), kind=wl.kind)
     q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
     out = torch.empty((H, N, D), dtype=torch.float32, device=dev)
     lse = torch.empty((H, N), dtype=torch.float32, device=dev)
@@ -298,12 +389,9 @@ def main():
     total_ms = t_start.elapsed_time(t_end)
     norms_ms = [e[0].elapsed_time(e[1]) for e in evs]
     attn_ms = [e[1].elapsed_time(e[2]) for e in evs]
-    if pg is not None:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, pg, dev)
     ms_step = total_ms / args.steps
-    value = flops_step * world * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(flops_step, world, args.steps, total_ms)
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
@@ -329,11 +417,8 @@ def main():
         b.record(stream)
         barrier()
         e2e_ms = a.elapsed_time(b)
-        if pg is not None:
-            t = torch.tensor([e2e_ms], device=dev)
-            pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": flops_step * world * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        e2e_ms = max_over_ranks(e2e_ms, pg, dev)
+        e2e = {"value": job_throughput(flops_step, world, e2e_steps, e2e_ms), "unit": UNIT,
                "h2d_bytes_per_step": 3 * H * N * D * 2, "d2h_bytes_per_step": H * N * D * 4 + H * N * 4,
                "ms_per_step": e2e_ms / e2e_steps,
                "path": "fsa_forward_host: pinned host q,k,v -> chunks of heads copied in, normed and attended, "
