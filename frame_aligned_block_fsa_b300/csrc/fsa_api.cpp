@@ -221,17 +221,18 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
         eligible = P->d_elig;
     }
     const int64_t rows = static_cast<int64_t>(H) * P->N;
-    CUtensorMap mk, mv;
+    CUtensorMap mq, mk, mv;
+    if ((rc = make_tensor_map(&mq, q, rows, D, 128)) != FSA_OK) return rc;
     if ((rc = make_tensor_map(&mk, k, rows, D, NK)) != FSA_OK) return rc;
     if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
     fsa::AttnLaunch L;
     L.D = D;
     L.NK = NK;
     L.H = H;
+    L.tmQ = &mq;
     L.tmK = &mk;
     L.tmV = &mv;
     L.stream = st;
-    L.params.q = q;
     L.params.items = P->d_items;
     L.params.runs = P->d_runs;
     L.params.n_items = P->n_items;

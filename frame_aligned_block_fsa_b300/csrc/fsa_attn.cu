@@ -11,30 +11,33 @@
 //    test take the running-max path inside the same kernel.
 //
 // B300 design (one CTA per SM, 18 warps, two 128-row query tiles j = 0, 1 of one frame):
-//   warps 0-7   query tile 0: load Q_0 into TMEM once, then per key tile the softmax and at
-//               the end the epilogue.  A thread owns one row (= TMEM lane); the two warps
-//               of a lane quarter (w and w + 4) split the key tile's 16-column chunks
-//               (even / odd), so a row's exponentials run in two warps at once.
+//   warps 0-7   query tile 0: per key tile the softmax, at the end the epilogue.  A thread
+//               owns one row (= TMEM lane); the two warps of a lane quarter (w and w + 4)
+//               split the key tile's 16-column chunks (even / odd), so a row's
+//               exponentials run in two warps at once.
 //   warps 8-15  the same for query tile 1
-//   warp 16     TMA producer: K and V tiles of up to NK keys through an NS-stage mbarrier
-//               ring (128-byte swizzled boxes)
+//   warp 16     TMA producer: the two query tiles once, then K and V tiles of up to NK keys
+//               through an NS-stage mbarrier ring (128-byte swizzled boxes)
 //   warp 17     allocates TMEM and issues tcgen05.mma (the warp runs the loop, one elected
 //               lane issues):
-//                 S_j  = Q_j K^T   (A = Q_j from TMEM, B = K tile from shared memory)
+//                 S_j  = Q_j K^T   (A = Q_j, B = K tile, both from shared memory)
 //                 O_j += P_j V     (A = P_j from TMEM, B = V tile from shared memory, MN-major)
-// The tensor pipe takes MMAs from a very short queue: an issuing thread stays blocked for
-// about as long as its MMAs take, and the pipe idles while the issuer waits.
-// Both products take A from TMEM.  With A in shared memory a 128 x 80 x 16 MMA reads 6.5 KB
-// of operands for 40 cycles of math, more than shared memory delivers (128 B/clk), which
-// slowed the MMAs and every other shared-memory access of the CTA, barriers included.
+//
+// Each query tile has two S buffers in TMEM, so the MMAs run two key tiles ahead of the
+// softmax: S_j(t+2) is issued right after PV_j(t), into the buffer PV_j(t) has just read P_j(t)
+// from.  The softmax therefore finds S_j(t+1) ready when it finishes tile t, and the chain
+// "softmax, hand-off, MMAs, hand-off back" no longer sets the pace; the tensor pipe and the
+// exponentials do.  (The tensor pipe takes MMAs from a very short queue, so an issuing thread
+// is blocked for about as long as its MMAs take; with one S buffer per tile the pipe idled
+// for every hand-off.)  Q stays in shared memory to leave TMEM for the second buffer.
 //
 // TMEM (512 columns): per query tile j a 256-column region
-//   [S_j: NK fp32 columns][Q_j: D/2][O_j: D fp32].
-// P_j(t) overwrites S_j(t) after the softmax has read it: the 8 bf16-pair columns of the 16
-// keys of S chunk c go to the first 8 columns of that chunk, so each warp overwrites only
-// columns it has read itself.  S_j(t+1) is issued after PV_j(t) by the same thread, and the
-// tensor pipe executes one thread's MMAs in issue order, so PV_j(t) has read P_j(t) before
-// S_j(t+1) overwrites it.
+//   [S_j buffer 0: NK fp32][S_j buffer 1: NK fp32][O_j: D fp32].
+// P_j(t) overwrites S_j(t) in its buffer after the softmax has read it: the 8 bf16-pair
+// columns of the 16 keys of S chunk c go to the first 8 columns of that chunk, so each warp
+// overwrites only columns it has read itself.  S_j(t+2) is issued after PV_j(t) by the same
+// thread, and the tensor pipe executes one thread's MMAs in issue order, so PV_j(t) has read
+// P_j(t) before S_j(t+2) overwrites it.
 //
 // Key tiles: each key run (a whole number of frames) is cut into tiles of NK keys and one
 // last narrower tile of the remaining len mod NK keys (a multiple of 16, since T is).  Every
@@ -58,31 +61,39 @@ struct AttnCfg {
     static_assert(NK % 16 == 0 && NK >= 16 && NK <= kMaxKeyTile(D), "key tile");
     static constexpr int BM = 128;                      // query rows per tile (MMA M)
     static constexpr int PANELS = D / 64;               // 64-element (128 B) swizzle panels
+    static constexpr int Q_PANEL_BYTES = BM * 128;
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
     static constexpr int KV_PANEL_BYTES = NK * 128;
     static constexpr int KV_TILE_BYTES = NK * D * 2;
     static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;  // K and V
     static constexpr int SMEM_LIMIT = 232448;              // max dynamic smem per block
     static constexpr int RESERVED = 256;                   // barriers + flags
-    static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - RESERVED) / STAGE_BYTES;
+    static constexpr int LSUM_BYTES = 2 * 2 * 128 * 4;     // row-sum halves (epilogue)
+    static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - RESERVED - LSUM_BYTES - 2 * Q_TILE_BYTES) / STAGE_BYTES;
     static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
-    static_assert(NS >= 2, "pipeline depth");
-    static constexpr int K_OFF = 0;
+    static_assert(NS >= 3, "pipeline depth: two key tiles ahead of the one being read");
+    static constexpr int Q_OFF = 0;
+    static constexpr int K_OFF = 2 * Q_TILE_BYTES;
     static constexpr int V_OFF = K_OFF + NS * KV_TILE_BYTES;
     static constexpr int BAR_OFF = V_OFF + NS * KV_TILE_BYTES;
     // barrier indices
-    static constexpr int B_KVFULL = 0;                // NS: K and V of a stage landed
+    static constexpr int B_QFULL = 0;
+    static constexpr int B_KVFULL = 1;                // NS: K and V of a stage landed
     static constexpr int B_KVEMPTY = B_KVFULL + NS;   // NS: the MMAs reading a stage are done
-    static constexpr int B_SFULL = B_KVEMPTY + NS;    // 2: S_j complete (and every MMA before it)
-    static constexpr int B_PVDONE = B_SFULL + 2;      // 2: the last PV_j complete
-    static constexpr int B_DRAIN = B_PVDONE + 2;
+    static constexpr int B_SFULL = B_KVEMPTY + NS;    // 4: S_j in buffer b complete (index 2 j + b)
+    static constexpr int B_PVDONE = B_SFULL + 4;      // 2: PV_j complete
+    // 4: P_j of a key tile in buffer b in TMEM (index 2 j + b, 8 arrivals).  One barrier per
+    // buffer: the softmax can finish key tile t+1 before the MMA warp has waited for tile t,
+    // but never tile t+2, so each barrier is at most one phase ahead of its waiter.
+    static constexpr int B_PFULL = B_PVDONE + 2;
+    static constexpr int B_DRAIN = B_PFULL + 4;
     static constexpr int N_BARS = B_DRAIN + 1;
-    // abort flag (+0), TMEM address (+8), ready counters of the two query tiles (+16, +20),
-    // row-sum exchange counters (+24, +28)
+    // abort flag (+0), TMEM address (+8), row-sum exchange counters (+16, +20)
     static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
-    static_assert(MISC_OFF + 32 <= BAR_OFF + RESERVED, "reserved area");
+    static_assert(MISC_OFF + 24 <= BAR_OFF + RESERVED, "reserved area");
     // per query tile, per column half, per row: the half's partial row sum (epilogue)
     static constexpr int LSUM_OFF = BAR_OFF + RESERVED;
-    static constexpr int SMEM_USED = 1024 + LSUM_OFF + 2 * 2 * 128 * 4;
+    static constexpr int SMEM_USED = 1024 + LSUM_OFF + LSUM_BYTES;
     // At least half of the SM's shared memory, so two CTAs never share an SM and contend for
     // its 512 TMEM columns.
     static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -90,17 +101,15 @@ struct AttnCfg {
     static_assert(KV_PANEL_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t REGION = 256;
-    static_assert(NK + D / 2 + D <= static_cast<int>(REGION), "TMEM budget");
-    static constexpr uint32_t t_s(int j) { return REGION * j; }
-    static constexpr uint32_t t_p(int j) { return REGION * j; }  // chunk c's P at t_p + 16 c
-    static constexpr uint32_t t_q(int j) { return REGION * j + NK; }
-    static constexpr uint32_t t_o(int j) { return REGION * j + NK + D / 2; }
+    static_assert(2 * NK + D <= static_cast<int>(REGION), "TMEM budget");
+    static constexpr uint32_t t_s(int j, int b) { return REGION * j + NK * b; }  // chunk c's P at + 16 c
+    static constexpr uint32_t t_o(int j) { return REGION * j + 2 * NK; }
     static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 };
 
 // wait sites (diagnostic codes in fsa_stats_t::timeout_site)
 enum : int {
-    SITE_PROD_EMPTY = 1, SITE_MMA_K = 3, SITE_MMA_Q = 4, SITE_MMA_P = 6, SITE_SOFT_S = 7, SITE_SOFT_O = 8,
+    SITE_PROD_EMPTY = 1, SITE_MMA_Q = 2, SITE_MMA_K = 3, SITE_MMA_P = 6, SITE_SOFT_S = 7, SITE_SOFT_O = 8,
     SITE_DRAIN = 9, SITE_SELFTEST = 10
 };
 
@@ -141,8 +150,8 @@ struct KeyTiles {
 
 template <int D, int NK>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                        const AttnParams p)
+    fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                        const __grid_constant__ CUtensorMap tmV, const AttnParams p)
 {
     using C = AttnCfg<D, NK>;
     extern __shared__ uint8_t smem_raw[];
@@ -152,10 +161,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::MISC_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
-    uint32_t* ready = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 16);
-    // ready[j] counts warp signals of query tile j: 8 once Q_j is in TMEM, then 8 more per
-    // key tile t once P_j(t) is in TMEM.
-    auto ready_addr = [&](int j) -> uint32_t { return sbase + C::MISC_OFF + 16u + 4u * static_cast<uint32_t>(j); };
+    uint32_t* xcount = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 16);
+    // xcount[j] counts the row-sum halves of query tile j written to shared memory
+    auto xcount_addr = [&](int j) -> uint32_t { return sbase + C::MISC_OFF + 16u + 4u * static_cast<uint32_t>(j); };
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -174,15 +182,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                            (p.eligible == nullptr || p.eligible[h] != 0);
 
     if (threadIdx.x == 0) {
+        mbar_init(bar(C::B_QFULL), 1);
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(bar(C::B_KVFULL + s), 1);
             mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
+        for (int i = 0; i < 4; ++i) mbar_init(bar(C::B_SFULL + i), 1);
         for (int j = 0; j < 2; ++j) {
-            mbar_init(bar(C::B_SFULL + j), 1);
             mbar_init(bar(C::B_PVDONE + j), 1);
-            ready[j] = 0;
-            ready[2 + j] = 0;
+            mbar_init(bar(C::B_PFULL + 2 * j), 8);  // one arrival per softmax warp of the tile
+            mbar_init(bar(C::B_PFULL + 2 * j + 1), 8);
+            xcount[j] = 0;
         }
         mbar_init(bar(C::B_DRAIN), 1);
         *abort_flag = 0;
@@ -207,9 +217,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == kWarpTma) {
         // ------------------------------------------------------------- TMA producer
         if (lane == 0) {
+            tma_prefetch_desc(&tmQ);
             tma_prefetch_desc(&tmK);
             tma_prefetch_desc(&tmV);
             const uint64_t pol_kv = policy_evict_last();
+            // Both query tiles in full (rows past the tensor are zero-filled; rows past the
+            // frame are computed but never stored).
+            mbar_arrive_expect_tx(bar(C::B_QFULL), static_cast<uint32_t>(nq * C::Q_TILE_BYTES));
+            for (int j = 0; j < nq; ++j)
+                for (int pn = 0; pn < C::PANELS; ++pn)
+                    tma_load_2d(sbase + C::Q_OFF + j * C::Q_TILE_BYTES + pn * C::Q_PANEL_BYTES, &tmQ, pn * 64,
+                                static_cast<int>(head_row0 + q_row0 + j * 128), bar(C::B_QFULL));
             KeyTiles<NK> tiles(runs);
             int t = 0;
             for (; t < n_tiles; ++t) {
@@ -229,99 +247,125 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      pn * 64, row, bar(C::B_KVFULL + st), pol_kv);
             }
             // Every copy this thread issued must land before the CTA may exit.
+            mbar_wait(bar(C::B_QFULL), 0, wc, SITE_DRAIN, false);
             for (int u = (t > C::NS ? t - C::NS : 0); u < t; ++u)
                 mbar_wait(bar(C::B_KVFULL + u % C::NS), (u / C::NS) & 1, wc, SITE_DRAIN, false);
         }
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------- MMA issuer
-        // Issue order per key tile t:  PV_0(t), S_0(t+1), PV_1(t), S_1(t+1).  While softmax j
-        // works on S_j(t+1) the pipe runs the other query tile's pair, so the two tiles keep
-        // the pipe busy in turn.  A commit arrives when every MMA its thread issued before it
-        // has completed, so S_j(t+1) being complete also means PV_j(t) is: P_j and O_j are
-        // free for the softmax.
+        // Prologue: S_j(0) into buffer 0 and S_j(1) into buffer 1 of every query tile j.  Per
+        // key tile t, for j = 0, 1: once softmax j has put P_j(t) into buffer t % 2, PV_j(t),
+        // then S_j(t+2) into the same buffer (the pipe runs one thread's MMAs in order).
+        // PVDONE_j is committed after every PV on running-max heads (the softmax rescales O_j
+        // only once PV_j(t-1) is done) and after the last PV on norm-bound heads.
         //
-        // The whole warp runs the loop, so the waits and the descriptor arithmetic stay
+        // The whole warp runs this loop, so the waits and the descriptor arithmetic stay
         // warp-uniform; one elected lane issues every tcgen05.mma and tcgen05.commit (a commit
-        // tracks the MMAs of its own thread, so the same lane issues all of them).  The next
-        // K/V stage's barrier is tested a tile ahead; the softmax hand-off is a shared counter.
+        // tracks the MMAs of its own thread, so the same lane issues all of them).
         const bool leader = elect_one();
         // Descriptor bases; moving the start address by b bytes adds b >> 4 to the descriptor.
+        const uint64_t dq = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
         const uint64_t dk = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
         const uint64_t dv = smem_desc_sw128(sbase + C::V_OFF, C::KV_PANEL_BYTES, 1024);
-        // S_j = Q_j K^T over the stage's keys (`probe` would run after half of the MMAs).
-        auto issue_s = [&](int j, int st, int width, auto&& probe) {
+        // S_j = Q_j K^T into buffer buf; `probe` runs after the first MMA is queued, so that the
+        // answer of an mbarrier test it issues is back by the time the group is queued.
+        auto issue_s = [&](int j, int buf, int st, int width, auto&& probe) {
+            const uint64_t a0 = dq + static_cast<uint64_t>((j * C::Q_TILE_BYTES) >> 4);
             const uint64_t b0 = dk + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
             const uint32_t idesc = idesc_bf16_f32(128, width, false, false);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks) {
-                if (ks == D / 32) probe();
+                if (ks == 1) probe();
                 // 16 bf16 = 32 B inside the 128 B swizzle row; a new 64-column panel every 4 steps
+                const uint32_t qo = ((ks >> 2) * C::Q_PANEL_BYTES + (ks & 3) * 32) >> 4;
                 const uint32_t ko = ((ks >> 2) * C::KV_PANEL_BYTES + (ks & 3) * 32) >> 4;
-                if (leader) mma_ts(tbase + C::t_s(j), tbase + C::t_q(j) + ks * 8, b0 + ko, idesc, ks > 0 ? 1u : 0u);
+                if (leader) mma_ss(tbase + C::t_s(j, buf), a0 + qo, b0 + ko, idesc, ks > 0 ? 1u : 0u);
             }
-            if (leader) tc_commit(bar(C::B_SFULL + j));
+            if (leader) tc_commit(bar(C::B_SFULL + 2 * j + buf));
             __syncwarp();
         };
-        auto issue_pv = [&](int j, int st, int width, bool first, bool last) {
+        auto no_probe = [] {};
+        auto issue_pv = [&](int j, int buf, int st, int width, bool first, bool commit) {
             const uint64_t b0 = dv + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
             if (leader) {
 #pragma unroll
                 for (int ks = 0; ks < NK / 16; ++ks)
                     if (ks < width / 16)
-                        mma_ts(tbase + C::t_o(j), tbase + C::t_p(j) + ks * 16, b0 + ((ks * 16 * 128) >> 4),
+                        mma_ts(tbase + C::t_o(j), tbase + C::t_s(j, buf) + ks * 16, b0 + ((ks * 16 * 128) >> 4),
                                C::IDESC_O, (!first || ks > 0) ? 1u : 0u);
-                if (last) tc_commit(bar(C::B_PVDONE + j));
+                if (commit) tc_commit(bar(C::B_PVDONE + j));
             }
             __syncwarp();
         };
-        auto stage_wait = [&](int t, bool pretested) -> bool {
-            if (__all_sync(0xffffffffu, pretested)) return true;
+        // An mbarrier test answers only after a long round trip while shared memory is busy,
+        // so readiness is tested early (the answer `seen`) and waited for only when it was no.
+        auto stage_test = [&](int t) { return mbar_test_wait(bar(C::B_KVFULL + t % C::NS), (t / C::NS) & 1); };
+        auto stage_wait = [&](int t, bool seen) -> bool {
+            if (__all_sync(0xffffffffu, seen)) return true;
             return __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVFULL + t % C::NS), (t / C::NS) & 1, wc, SITE_MMA_K));
         };
-        // readiness of query tile j for key tile t (Q_j and P_j(0..t) in TMEM)
-        auto p_target = [](int t) { return 8u * static_cast<uint32_t>(t + 2); };
+        auto p_test = [&](int j, int t) { return mbar_test_wait(bar(C::B_PFULL + 2 * j + (t & 1)), (t >> 1) & 1); };
         auto p_wait = [&](int j, int t, bool seen) -> bool {
             if (__all_sync(0xffffffffu, seen)) return true;
-            return __all_sync(0xffffffffu, counter_wait(ready_addr(j), p_target(t), wc, SITE_MMA_P));
+            return __all_sync(0xffffffffu, mbar_wait(bar(C::B_PFULL + 2 * j + (t & 1)), (t >> 1) & 1, wc, SITE_MMA_P));
         };
-        auto no_probe = [] {};
+        // widths of tiles t, t+1, t+2 (w_cur, w_1, w_2)
         KeyTiles<NK> tiles(runs);
-        int start, w_cur = 0, w_next = 0;
+        int start, w_cur = 0, w_1 = 0, w_2 = 0;
         bool ok = n_tiles > 0;
         if (ok) {
             tiles.next(start, w_cur);
-            ok = stage_wait(0, false);
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_QFULL), 0, wc, SITE_MMA_Q));
         }
-        for (int j = 0; j < nq && ok; ++j) {
-            if (!(ok = __all_sync(0xffffffffu, counter_wait(ready_addr(j), 8u, wc, SITE_MMA_Q)))) break;
+        if (ok) ok = stage_wait(0, false);
+        if (ok) {
             tc_fence_after();
-            issue_s(j, 0, w_cur, no_probe);
+            for (int j = 0; j < nq; ++j) issue_s(j, 0, 0, w_cur, no_probe);
         }
-        bool next_ready = false;  // answer of an early test of the stage of tile t+1
-        if (ok && n_tiles > 1) next_ready = mbar_test_wait(bar(C::B_KVFULL + 1 % C::NS), (1 / C::NS) & 1);
+        if (ok && n_tiles > 1) {
+            tiles.next(start, w_1);
+            if ((ok = stage_wait(1, false))) {
+                tc_fence_after();
+                for (int j = 0; j < nq; ++j) issue_s(j, 1, 1, w_1, no_probe);
+            }
+        }
+        bool p_seen[2] = {false, false};  // early answers: P_j(t) ready
+        bool st_seen = false;             // early answer: the stage of tile t+2 landed
+        if (ok && n_tiles > 2) st_seen = stage_test(2);
         for (int t = 0; t < n_tiles && ok; ++t) {
             const int st = t % C::NS;
-            const int st1 = (t + 1) % C::NS;
-            const bool next = t + 1 < n_tiles;
-            if (next) tiles.next(start, w_next);
-            bool ready2 = false;
+            const int buf = t & 1;
+            const bool ahead = t + 2 < n_tiles;
+            if (ahead) tiles.next(start, w_2);
+            const bool last = t + 1 == n_tiles;
+            bool st_next = false;
             for (int j = 0; j < nq && ok; ++j) {
-                if (!(ok = p_wait(j, t, false))) break;
+                if (!(ok = p_wait(j, t, p_seen[j]))) break;
                 tc_fence_after();
-                issue_pv(j, st, w_cur, t == 0, !next);
-                if (next) {
-                    if (j == 0) {
-                        if (!(ok = stage_wait(t + 1, next_ready))) break;
-                        tc_fence_after();
-                        if (t + 2 < n_tiles)
-                            ready2 = mbar_test_wait(bar(C::B_KVFULL + (t + 2) % C::NS), ((t + 2) / C::NS) & 1);
+                issue_pv(j, buf, st, w_cur, t == 0, last || !use_bound);
+                // while S_j(t+2) is queued: ask about the next group's P and the stage after next
+                auto probe = [&] {
+                    if (j + 1 < nq) {
+                        p_seen[j + 1] = p_test(j + 1, t);
+                    } else {
+                        p_seen[0] = t + 1 < n_tiles && p_test(0, t + 1);
+                        st_next = t + 3 < n_tiles && stage_test(t + 3);
                     }
-                    issue_s(j, st1, w_next, no_probe);
+                };
+                if (ahead) {
+                    if (j == 0) {
+                        if (!(ok = stage_wait(t + 2, st_seen))) break;
+                        tc_fence_after();
+                    }
+                    issue_s(j, buf, (t + 2) % C::NS, w_2, probe);
+                } else {
+                    probe();
                 }
             }
             if (!ok) break;
-            next_ready = ready2;
-            w_cur = w_next;
+            st_seen = st_next;
+            w_cur = w_1;
+            w_1 = w_2;
             if (leader) tc_commit(bar(C::B_KVEMPTY + st));
             __syncwarp();
         }
@@ -341,34 +385,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const bool rv = row < valid;
             const int64_t grow = head_row0 + q_row0 + 128 * j + row;
             const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
-            const uint32_t tS = tbase + lane_off + C::t_s(j);
-            const uint32_t tP = tbase + lane_off + C::t_p(j);
-            const uint32_t tQ = tbase + lane_off + C::t_q(j);
             const uint32_t tO = tbase + lane_off + C::t_o(j) + hf * (D / 2);  // this warp's half of O
             constexpr int OWN = (NK / 16 + 1) / 2;  // most chunks a warp owns
-            // Q_j into TMEM: the row as D/2 columns of bf16 pairs (the layout of an MMA A
-            // operand in TMEM), this warp's half of them; rows past the frame's last token are 0.
-            {
-                const uint4* qrow = reinterpret_cast<const uint4*>(p.q + grow * D) + hf * (D / 16);
-#pragma unroll
-                for (int c = 0; c < D / 64; ++c) {
-                    uint32_t qw[16];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const uint4 u = rv ? __ldg(qrow + 4 * c + e) : make_uint4(0u, 0u, 0u, 0u);
-                        qw[4 * e] = u.x;
-                        qw[4 * e + 1] = u.y;
-                        qw[4 * e + 2] = u.z;
-                        qw[4 * e + 3] = u.w;
-                    }
-                    tmem_st_x8(tQ + hf * (D / 4) + 16 * c, qw);
-                    tmem_st_x8(tQ + hf * (D / 4) + 16 * c + 8, qw + 8);
-                }
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) red_release_shared_add(ready_addr(j), 1u);
-            }
             const float c2 = rv ? p.scale_log2 : 0.0f;
             const float b_nat = (rv && p.bound) ? p.bound[grow] : 0.0f;
             const float nb2 = use_bound ? -b_nat * kLog2e : 0.0f;
@@ -380,8 +398,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 int start, width;
                 tiles.next(start, width);
                 const int nch = width / 16;  // 16-column chunks of this tile
+                const int buf = t & 1;
+                const uint32_t tS = tbase + lane_off + C::t_s(j, buf);
                 // the vote keeps the warp converged for the warp-collective TMEM accesses
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + j), t & 1, wc, SITE_SOFT_S)))) break;
+                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + 2 * j + buf), (t >> 1) & 1, wc,
+                                                             SITE_SOFT_S))))
+                    break;
                 tc_fence_after();
                 float s[16 * OWN];  // own chunks, compact
                 uint32_t pk[8 * OWN];
@@ -431,37 +453,45 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                 }
                 l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
-                // S_j(t) complete means PV_j(t-1) is too (issued before it): O_j may be
-                // rescaled and P_j(t) may overwrite S_j(t) now.
-                if (!use_bound && t > 0 && __any_sync(0xffffffffu, m_new > m2)) {
-                    // running max moved: rescale this warp's half of the accumulator before
-                    // PV_j(t) may start
+                if (!use_bound && t > 0) {
+                    // O_j may be rescaled only once PV_j(t-1) is done (committed every tile here)
+                    if (!(ok = __all_sync(0xffffffffu,
+                                          mbar_wait(bar(C::B_PVDONE + j), (t - 1) & 1, wc, SITE_SOFT_O))))
+                        break;
+                    tc_fence_after();
+                    if (__any_sync(0xffffffffu, m_new > m2)) {
+                        // running max moved: rescale this warp's half of the accumulator before
+                        // PV_j(t) may start
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        float o[16];
-                        tmem_load_cols<16>(tO + 16 * c, o);
+                        for (int c = 0; c < D / 32; ++c) {
+                            float o[16];
+                            tmem_load_cols<16>(tO + 16 * c, o);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) o[e] *= alpha;
-                        tmem_st_x16(tO + 16 * c, o);
+                            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+                            tmem_st_x16(tO + 16 * c, o);
+                        }
                     }
                 }
                 m2 = m_new;
 #pragma unroll
                 for (int i = 0; i < OWN; ++i)
-                    if (2 * i + hf < nch) tmem_st_x8(tP + 16 * (2 * i + hf), pk + 8 * i);
+                    if (2 * i + hf < nch) tmem_st_x8(tS + 16 * (2 * i + hf), pk + 8 * i);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) red_release_shared_add(ready_addr(j), 1u);
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + 2 * j + buf));
             }
+            // the last PV: phase n_tiles - 1 on running-max heads (every PV committed), the
+            // only phase 0 on norm-bound heads
             if (ok && n_tiles > 0)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + j), 0, wc, SITE_SOFT_O));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + j), use_bound ? 0 : (n_tiles - 1) & 1, wc,
+                                                       SITE_SOFT_O));
             // The row sum is split over the two warps of the row: exchange the halves.
             float* lsum = reinterpret_cast<float*>(sgen + C::LSUM_OFF) + (2 * j) * 128;
             lsum[hf * 128 + row] = l;
             __syncwarp();
-            if (lane == 0) red_release_shared_add(ready_addr(2 + j), 1u);
-            if (ok) ok = __all_sync(0xffffffffu, counter_wait(ready_addr(2 + j), 8u, wc, SITE_SOFT_O));
+            if (lane == 0) red_release_shared_add(xcount_addr(j), 1u);
+            if (ok) ok = __all_sync(0xffffffffu, counter_wait(xcount_addr(j), 8u, wc, SITE_SOFT_O));
             if (ok) {
                 tc_fence_after();
                 const float l_row = l + lsum[(1 - hf) * 128 + row];
@@ -540,7 +570,7 @@ static int launch_attn(const AttnLaunch& L)
         attr_done = true;
     }
     const dim3 grid(static_cast<unsigned>(L.params.n_items) * static_cast<unsigned>(L.H));
-    kern<<<grid, kAttnThreads, C::SMEM_BYTES, L.stream>>>(*L.tmK, *L.tmV, L.params);
+    kern<<<grid, kAttnThreads, C::SMEM_BYTES, L.stream>>>(*L.tmQ, *L.tmK, *L.tmV, L.params);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 

@@ -14,13 +14,12 @@ namespace fsa {
 constexpr int kMaxRuns = 4;
 
 // Largest key tile the attention kernel supports (for D = 64 and 128): each of the two query
-// tiles holds S and P (NK columns), Q (D/2 columns) and O (D columns) in 256 TMEM columns,
-// and a softmax thread keeps its half of a tile row in registers.
+// tiles holds two S buffers (NK columns each, P written over S) and O (D columns) in 256 TMEM
+// columns, and a softmax thread keeps its half of a tile row in registers.
 constexpr int kMaxKeyTile(int D) { return 64; }
 constexpr int kRunStride = 1 + 2 * kMaxRuns;
 
 struct AttnParams {
-    const uint16_t* q;     // bf16 [H][N][D]
     const int32_t* items;  // [n_items][4]: query frame, first query row (token), valid rows tile 0, tile 1
     const int32_t* runs;   // [F][kRunStride]
     int n_items;
@@ -38,6 +37,7 @@ struct AttnParams {
 
 struct AttnLaunch {
     int D, NK, H;
+    const CUtensorMap* tmQ;
     const CUtensorMap* tmK;
     const CUtensorMap* tmV;
     AttnParams params;
