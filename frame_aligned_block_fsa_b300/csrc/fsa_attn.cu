@@ -129,16 +129,27 @@ __device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* v)
     for (int i = 0; i < W; ++i) reg_fence(v[i]);
 }
 
-// Walks a query frame's key runs in tiles of at most NK keys: (first key, width).
+// Walks a query frame's key runs in tiles of at most NK keys: (first key, width).  The runs
+// (at most kMaxRuns) are read once into registers, so that stepping costs no memory access.
 template <int NK>
 struct KeyTiles {
-    const int32_t* runs;
+    int s0 = 0, s1 = 0, s2 = 0, s3 = 0, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
     int r = 0, k0 = 0;
-    __device__ explicit KeyTiles(const int32_t* rr) : runs(rr) {}
+    __device__ explicit KeyTiles(const int32_t* rr)
+    {
+        static_assert(kMaxRuns == 4, "one register pair per run");
+        const int n = rr[0];
+        s0 = rr[1];
+        l0 = rr[2];
+        if (n > 1) { s1 = rr[3]; l1 = rr[4]; }
+        if (n > 2) { s2 = rr[5]; l2 = rr[6]; }
+        if (n > 3) { s3 = rr[7]; l3 = rr[8]; }
+    }
     __device__ __forceinline__ void next(int& start, int& width)
     {
-        const int len = runs[2 + 2 * r];
-        start = runs[1 + 2 * r] + k0;
+        const int len = r == 0 ? l0 : (r == 1 ? l1 : (r == 2 ? l2 : l3));
+        const int base = r == 0 ? s0 : (r == 1 ? s1 : (r == 2 ? s2 : s3));
+        start = base + k0;
         width = min(NK, len - k0);
         k0 += width;
         if (k0 == len) {
