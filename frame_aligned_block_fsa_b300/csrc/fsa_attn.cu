@@ -69,7 +69,8 @@ struct AttnCfg {
     static constexpr int SMEM_LIMIT = 232448;              // max dynamic smem per block
     static constexpr int RESERVED = 256;                   // barriers + flags
     static constexpr int LSUM_BYTES = 2 * 2 * 128 * 4;     // row-sum halves (epilogue)
-    static constexpr int NS_FIT = (SMEM_LIMIT - 1024 - RESERVED - LSUM_BYTES - 2 * Q_TILE_BYTES) / STAGE_BYTES;
+    static constexpr int NS_FIT =
+        (SMEM_LIMIT - 1024 - RESERVED - LSUM_BYTES - 2 * 2 * 2 * 128 * 4 - 2 * Q_TILE_BYTES) / STAGE_BYTES;
     static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
     static_assert(NS >= 3, "pipeline depth: two key tiles ahead of the one being read");
     static constexpr int Q_OFF = 0;
@@ -88,12 +89,16 @@ struct AttnCfg {
     static constexpr int B_PFULL = B_PVDONE + 2;
     static constexpr int B_DRAIN = B_PFULL + 4;
     static constexpr int N_BARS = B_DRAIN + 1;
-    // abort flag (+0), TMEM address (+8), row-sum exchange counters (+16, +20)
+    // abort flag (+0), TMEM address (+8), row-sum exchange counters (+16, +20), row-max
+    // exchange counters per (query tile, lane quarter) (+24 .. +56)
     static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
-    static_assert(MISC_OFF + 24 <= BAR_OFF + RESERVED, "reserved area");
+    static_assert(MISC_OFF + 56 <= BAR_OFF + RESERVED, "reserved area");
     // per query tile, per column half, per row: the half's partial row sum (epilogue)
     static constexpr int LSUM_OFF = BAR_OFF + RESERVED;
-    static constexpr int SMEM_USED = 1024 + LSUM_OFF + LSUM_BYTES;
+    // per key-tile parity, query tile, column half, row: the half's tile max (running-max path)
+    static constexpr int MMAX_OFF = LSUM_OFF + LSUM_BYTES;
+    static constexpr int MMAX_BYTES = 2 * 2 * 2 * 128 * 4;
+    static constexpr int SMEM_USED = 1024 + MMAX_OFF + MMAX_BYTES;
     // At least half of the SM's shared memory, so two CTAs never share an SM and contend for
     // its 512 TMEM columns.
     static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
@@ -199,6 +204,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(bar(C::B_KVEMPTY + s), 1);
         }
         for (int i = 0; i < 4; ++i) mbar_init(bar(C::B_SFULL + i), 1);
+        for (int i = 0; i < 8; ++i) xcount[2 + i] = 0;
         for (int j = 0; j < 2; ++j) {
             mbar_init(bar(C::B_PVDONE + j), 1);
             mbar_init(bar(C::B_PFULL + 2 * j), 8);  // one arrival per softmax warp of the tile
@@ -340,43 +346,60 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int j = 0; j < nq; ++j) issue_s(j, 1, 1, w_1, no_probe);
             }
         }
-        bool p_seen[2] = {false, false};  // early answers: P_j(t) ready
-        bool st_seen = false;             // early answer: the stage of tile t+2 landed
-        if (ok && n_tiles > 2) st_seen = stage_test(2);
+        bool p_seen0 = false, p_seen1 = false;  // early answers: P_0(t), P_1(t) ready
+        bool st_seen = n_tiles > 2 && ok && stage_test(2);  // early answer: tile t+2's stage landed
+        // Loop state of key tile t: width of tile t+2 (w_2), read in the previous iteration so
+        // that the next group's bookkeeping runs while MMAs of the current group are queued.
+        bool ahead = n_tiles > 2;
+        if (ahead) tiles.next(start, w_2);
         for (int t = 0; t < n_tiles && ok; ++t) {
             const int st = t % C::NS;
             const int buf = t & 1;
-            const bool ahead = t + 2 < n_tiles;
-            if (ahead) tiles.next(start, w_2);
             const bool last = t + 1 == n_tiles;
+            const bool pv_commit = last || !use_bound;
             bool st_next = false;
-            for (int j = 0; j < nq && ok; ++j) {
-                if (!(ok = p_wait(j, t, p_seen[j]))) break;
+            bool ahead_next = false;
+            int w_3 = 0;
+            // the work of the next key tile's loop head, done between MMAs of the last group
+            auto advance = [&] {
+                p_seen0 = t + 1 < n_tiles && p_test(0, t + 1);
+                st_next = t + 3 < n_tiles && stage_test(t + 3);
+                ahead_next = t + 3 < n_tiles;
+                if (ahead_next) tiles.next(start, w_3);
+            };
+            // query tile 0
+            if (!(ok = p_wait(0, t, p_seen0))) break;
+            tc_fence_after();
+            issue_pv(0, buf, st, w_cur, t == 0, pv_commit);
+            if (ahead) {
+                if (!(ok = stage_wait(t + 2, st_seen))) break;
                 tc_fence_after();
-                issue_pv(j, buf, st, w_cur, t == 0, last || !use_bound);
-                // while S_j(t+2) is queued: ask about the next group's P and the stage after next
-                auto probe = [&] {
-                    if (j + 1 < nq) {
-                        p_seen[j + 1] = p_test(j + 1, t);
-                    } else {
-                        p_seen[0] = t + 1 < n_tiles && p_test(0, t + 1);
-                        st_next = t + 3 < n_tiles && stage_test(t + 3);
-                    }
-                };
-                if (ahead) {
-                    if (j == 0) {
-                        if (!(ok = stage_wait(t + 2, st_seen))) break;
-                        tc_fence_after();
-                    }
-                    issue_s(j, buf, (t + 2) % C::NS, w_2, probe);
-                } else {
-                    probe();
-                }
             }
-            if (!ok) break;
+            auto probe0 = [&] {
+                if (nq > 1)
+                    p_seen1 = p_test(1, t);
+                else
+                    advance();
+            };
+            if (ahead)
+                issue_s(0, buf, (t + 2) % C::NS, w_2, probe0);
+            else
+                probe0();
+            // query tile 1
+            if (nq > 1) {
+                if (!(ok = p_wait(1, t, p_seen1))) break;
+                tc_fence_after();
+                issue_pv(1, buf, st, w_cur, t == 0, pv_commit);
+                if (ahead)
+                    issue_s(1, buf, (t + 2) % C::NS, w_2, advance);
+                else
+                    advance();
+            }
             st_seen = st_next;
+            ahead = ahead_next;
             w_cur = w_1;
             w_1 = w_2;
+            w_2 = w_3;
             if (leader) tc_commit(bar(C::B_KVEMPTY + st));
             __syncwarp();
         }
@@ -429,8 +452,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 float alpha = 1.0f, m_new = m2;
                 float2 off = make_float2(nb2, nb2);
                 if (!use_bound) {
-                    // the running max over the whole row: both warps of the row compute it,
-                    // reading the other warp's chunks one at a time
+                    // The running max over the whole row.  The two warps of the row exchange
+                    // the maxima of their own chunks through shared memory: reading the other
+                    // warp's chunks from TMEM could race with its P being written over them.
                     float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int i = 0; i < OWN; ++i) {
@@ -438,14 +462,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                             for (int e = 0; e < 16; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[16 * i + e]);
                         }
-                        if (2 * i + 1 - hf < nch) {
-                            float so[16];
-                            tmem_load_cols<16>(tS + 16 * (2 * i + 1 - hf), so);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) mx[e & 3] = fmaxf(mx[e & 3], so[e]);
-                        }
                     }
-                    m_new = fmaxf(m2, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * c2);
+                    const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+                    // slots double-buffered by key-tile parity: a warp writes tile t+2's slot only
+                    // after its partner has written tile t+1's, i.e. after it read tile t's
+                    float* mslot = reinterpret_cast<float*>(sgen + C::MMAX_OFF) + (((t & 1) * 2 + j) * 2) * 128;
+                    mslot[hf * 128 + row] = mine;
+                    __syncwarp();
+                    const uint32_t xa = sbase + C::MISC_OFF + 24u + 4u * static_cast<uint32_t>(4 * j + quarter);
+                    if (lane == 0) red_release_shared_add(xa, 1u);
+                    if (!(ok = __all_sync(0xffffffffu,
+                                          counter_wait(xa, 2u * static_cast<uint32_t>(t + 1), wc, SITE_SOFT_S))))
+                        break;
+                    const float theirs = mslot[(1 - hf) * 128 + row];
+                    m_new = fmaxf(m2, fmaxf(mine, theirs) * c2);
                     alpha = ex2(m2 - m_new);
                     off = make_float2(-m_new, -m_new);
                 }
