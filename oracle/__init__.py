@@ -65,7 +65,7 @@ def _load():
             lib.oracle_attention_rows.argtypes = ([vp] * 3 + [i32] * 6 + [dbl, i64, vp, vp]
                                                   + [vp] * 6 + [i32])
             lib.oracle_attention_rows.restype = i32
-            lib.oracle_norms.argtypes = [vp] * 2 + [i32] * 6 + [dbl, dbl] + [vp] * 5
+            lib.oracle_norms.argtypes = [vp] * 2 + [i32] * 6 + [dbl, dbl, i32] + [vp] * 5
             lib.oracle_norms.restype = i32
             _lib = lib
     return _lib
@@ -169,8 +169,11 @@ def attention_full(q, k, v, F: int, T: int, w: int, ref: int, scale: float | Non
 
 
 def norms(q, k, F: int, T: int, w: int, ref: int, scale: float | None = None,
-          tau: float = DEFAULT_TAU) -> dict:
-    """Per-row norms, per-frame max key norms, row bounds, gap upper bounds, eligibility."""
+          tau: float = DEFAULT_TAU, center: bool = False) -> dict:
+    """Per-row norms, per-frame max key norms, row bounds, gap upper bounds, eligibility.
+
+    center=True measures key norms about the head's mean key and adds c <q, mu> back
+    into the bound (mean-centred keys)."""
     qb, kb = _bits(q), _bits(k)
     H, N, D = qb.shape
     assert N == F * T and kb.shape == qb.shape
@@ -178,7 +181,7 @@ def norms(q, k, F: int, T: int, w: int, ref: int, scale: float | None = None,
         scale = 1.0 / math.sqrt(D)
     res = {"qnorm": np.zeros((H, N)), "kmax": np.zeros((H, F)), "bound": np.zeros((H, N)),
            "gap_hat": np.zeros((H, N)), "eligible": np.zeros(H, dtype=np.uint8)}
-    rc = _load().oracle_norms(_ptr(qb), _ptr(kb), H, F, T, D, w, ref, float(scale), float(tau),
+    rc = _load().oracle_norms(_ptr(qb), _ptr(kb), H, F, T, D, w, ref, float(scale), float(tau), int(bool(center)),
                               _ptr(res["qnorm"]), _ptr(res["kmax"]), _ptr(res["bound"]),
                               _ptr(res["gap_hat"]), _ptr(res["eligible"]))
     if rc != 0:

@@ -313,25 +313,48 @@ int oracle_attention_rows(const uint16_t* q, const uint16_t* k, const uint16_t* 
  * with kbar_S the mean of all keys the row attends, bounds the gap
  * bound - rowmax from above.  A head is eligible iff max_n gap_hat <= tau;
  * then no row can push exp(s - bound) below exp(-tau).
+ *
+ * Mean-centred keys (same section: subtracting the key mean first tightens the
+ * bound because keys share a large common component, and the softmax does not
+ * see it).  Reading of this build: one mean per head over all N keys,
+ *   mu_h = (1/N) sum_n k_{h,n},
+ * and with center != 0
+ *   kmax[h][g]  = max over the keys n of frame g of ||k_{h,n} - mu_h||
+ *   bound[h][n] = c * (qnorm[h][n] * max_{g in S(f(n))} kmax[h][g] + <q_n, mu_h>),
+ * which is Cauchy-Schwarz on the centred logit c <q, k - mu> plus the row
+ * constant c <q, mu> added back, so it bounds the uncentred logits and the
+ * lse needs no correction.  gap_hat is bound - c <q_n, kbar_S> in both cases.
  * ------------------------------------------------------------------------- */
 int oracle_norms(const uint16_t* q, const uint16_t* k, int H, int F, int T, int D,
-                 int w, int ref, double scale, double tau,
+                 int w, int ref, double scale, double tau, int center,
                  double* qnorm, double* kmax, double* bound, double* gap_hat,
                  uint8_t* eligible)
 {
     if (H <= 0 || F <= 0 || T <= 0 || D <= 0 || w < 0 || ref < 0 || ref >= F) return -1;
     const int64_t N = (int64_t)F * T;
     double* kbar = (double*)malloc(sizeof(double) * (size_t)D);
-    if (!kbar) return -1;
+    double* mu = (double*)malloc(sizeof(double) * (size_t)D);
+    if (!kbar || !mu) {
+        free(kbar);
+        free(mu);
+        return -1;
+    }
     for (int h = 0; h < H; ++h) {
         const uint16_t* qh = q + (int64_t)h * N * D;
         const uint16_t* kh = k + (int64_t)h * N * D;
+        /* the head's key mean (left at zero without centring) */
+        for (int d = 0; d < D; ++d) mu[d] = 0.0;
+        if (center) {
+            for (int64_t n = 0; n < N; ++n)
+                for (int d = 0; d < D; ++d) mu[d] += bf16_to_double(kh[n * D + d]);
+            for (int d = 0; d < D; ++d) mu[d] /= (double)N;
+        }
         for (int g = 0; g < F; ++g) {
             double mx = 0.0;
             for (int64_t n = (int64_t)g * T; n < (int64_t)(g + 1) * T; ++n) {
                 double s2 = 0.0;
                 for (int d = 0; d < D; ++d) {
-                    double x = bf16_to_double(kh[n * D + d]);
+                    double x = bf16_to_double(kh[n * D + d]) - mu[d];
                     s2 += x * x;
                 }
                 double kn = sqrt(s2);
@@ -350,7 +373,7 @@ int oracle_norms(const uint16_t* q, const uint16_t* k, int H, int F, int T, int 
                 double s2 = 0.0;
                 for (int d = 0; d < D; ++d) {
                     double x = bf16_to_double(kh[j * D + d]);
-                    s2 += x * x;
+                    s2 += (x - mu[d]) * (x - mu[d]);
                     kbar[d] += x;
                 }
                 double kn = sqrt(s2);
@@ -359,22 +382,29 @@ int oracle_norms(const uint16_t* q, const uint16_t* k, int H, int F, int T, int 
             }
             for (int d = 0; d < D; ++d) kbar[d] /= (double)count;
             for (int64_t n = (int64_t)f * T; n < (int64_t)(f + 1) * T; ++n) {
-                double s2 = 0.0, dot = 0.0;
+                double s2 = 0.0, dot = 0.0, qmu = 0.0;
                 for (int d = 0; d < D; ++d) {
                     double x = bf16_to_double(qh[n * D + d]);
                     s2 += x * x;
                     dot += x * kbar[d];
+                    qmu += x * mu[d];
                 }
                 double qn = sqrt(s2);
                 int64_t at = (int64_t)h * N + n;
                 qnorm[at] = qn;
-                bound[at] = scale * qn * K;
-                gap_hat[at] = scale * (qn * K - dot);
+                if (center) {
+                    bound[at] = scale * (qn * K + qmu);
+                    gap_hat[at] = scale * (qn * K + qmu - dot);
+                } else {
+                    bound[at] = scale * qn * K;
+                    gap_hat[at] = scale * (qn * K - dot);
+                }
                 if (gap_hat[at] > worst) worst = gap_hat[at];
             }
         }
         eligible[h] = (uint8_t)(worst <= tau);
     }
     free(kbar);
+    free(mu);
     return 0;
 }

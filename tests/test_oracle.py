@@ -279,6 +279,75 @@ def test_norms_against_library_routines_and_gap_bound(oracle_mod, kind):
         assert e.tolist() == [int(x <= tau) for x in nm["gap_hat"].max(axis=1)]
 
 
+def test_centred_norms_hand_derived(oracle_mod):
+    # D=1, T=1, scale 1, w=0, reference frame 0.  Keys 1, 2, 6: head mean mu = 3, centred
+    # key norms |k - mu| = 2, 1, 3.  Queries 1, -1, 2.
+    #   frame 0: S = {0}     Kc = 2  bound = 1*2 + 1*3 = 5      kbar = 1    gap_hat = 5 - 1 = 4
+    #   frame 1: S = {0, 1}  Kc = 2  bound = 1*2 + (-1)*3 = -1  kbar = 1.5  gap_hat = -1 + 1.5 = 0.5
+    #   frame 2: S = {0, 2}  Kc = 3  bound = 2*3 + 2*3 = 12     kbar = 3.5  gap_hat = 12 - 7 = 5
+    # Row maxima: 1, -1, 12 (frames 1 and 2 meet their centred bound exactly).  Without
+    # centring the bounds are 1*1, 1*2, 2*6 and the key maxima 1, 2, 6.
+    q = _bf16([1, -1, 2]).reshape(1, 3, 1)
+    k = _bf16([1, 2, 6]).reshape(1, 3, 1)
+    c = oracle_mod.norms(q, k, F=3, T=1, w=0, ref=0, scale=1.0, tau=4.5, center=True)
+    np.testing.assert_allclose(c["kmax"][0], [2.0, 1.0, 3.0], atol=1e-15)
+    np.testing.assert_allclose(c["bound"][0], [5.0, -1.0, 12.0], atol=1e-15)
+    np.testing.assert_allclose(c["gap_hat"][0], [4.0, 0.5, 5.0], atol=1e-15)
+    assert c["eligible"].tolist() == [0]
+    u = oracle_mod.norms(q, k, F=3, T=1, w=0, ref=0, scale=1.0, center=False)
+    np.testing.assert_allclose(u["kmax"][0], [1.0, 2.0, 6.0], atol=1e-15)
+    np.testing.assert_allclose(u["bound"][0], [1.0, 2.0, 12.0], atol=1e-15)
+    att = oracle_mod.attention_full(q, k, k, F=3, T=1, w=0, ref=0, scale=1.0)
+    np.testing.assert_allclose(att["rowmax"][0], [1.0, -1.0, 12.0], atol=1e-15)
+
+
+def _integer_keys(H, N, D, seed, offset):
+    # small integers: every sum below is exact in bf16 and fp64
+    g = np.random.default_rng(seed)
+    z = g.integers(-4, 5, size=(H, N, D)).astype(np.float32)
+    m = g.integers(-offset, offset + 1, size=(H, 1, D)).astype(np.float32)
+    return z, m
+
+
+def test_centred_bound_is_translation_invariant(oracle_mod):
+    # Shifting every key of a head by one vector m moves each centred bound by exactly
+    # c <q, m> and leaves the centred key norms and the gap bound unchanged; the uncentred
+    # bound has no such property.  The centred bound still bounds the brute-force row max.
+    H, F, T, D, w, ref = 2, 6, 16, 32, 1, 3
+    z, m = _integer_keys(H, F * T, D, seed=5, offset=40)
+    q, _, v = make_qkv(H, F * T, D, seed=22)
+    k0, k1 = _bf16(z), _bf16(z + m)
+    assert torch.equal(k1.float(), torch.tensor(z + m))  # the shifted keys are exact
+    n0 = oracle_mod.norms(q, k0, F, T, w, ref, center=True)
+    n1 = oracle_mod.norms(q, k1, F, T, w, ref, center=True)
+    c = 1.0 / math.sqrt(D)
+    qm = np.einsum("hnd,hd->hn", _f64(q), m[:, 0, :].astype(np.float64))
+    np.testing.assert_allclose(n1["kmax"], n0["kmax"], rtol=1e-12)
+    np.testing.assert_allclose(n1["bound"] - n0["bound"], c * qm, atol=1e-9)
+    np.testing.assert_allclose(n1["gap_hat"], n0["gap_hat"], atol=1e-9)
+    att = oracle_mod.attention_full(q, k1, v, F, T, w, ref)
+    assert np.all(n1["bound"] >= att["rowmax"] - 1e-9)
+    assert np.all(n1["gap_hat"] >= n1["bound"] - att["rowmax"] - 1e-9)
+    # the common component inflates the uncentred gap bound, not the centred one
+    u1 = oracle_mod.norms(q, k1, F, T, w, ref, center=False)
+    assert n1["gap_hat"].max() < 0.5 * u1["gap_hat"].max()
+
+
+def test_centred_equals_uncentred_for_zero_mean_keys(oracle_mod):
+    # keys in +-pairs: the head mean is exactly zero, so centring changes nothing
+    H, F, T, D, w, ref = 2, 4, 16, 64, 1, 0
+    q, k, _ = make_qkv(H, F * T, D, seed=23)
+    kk = k.clone()
+    kk[:, 1::2, :] = -k[:, 0::2, :]
+    a = oracle_mod.norms(q, kk, F, T, w, ref, tau=10.0, center=True)
+    b = oracle_mod.norms(q, kk, F, T, w, ref, tau=10.0, center=False)
+    for name in ("qnorm", "kmax", "gap_hat", "eligible"):
+        np.testing.assert_array_equal(a[name], b[name])
+    np.testing.assert_allclose(a["bound"], b["bound"], rtol=1e-15)
+    for tau in (0.5, 5.0, 50.0):
+        e = oracle_mod.norms(q, kk, F, T, w, ref, tau=tau, center=True)["eligible"]
+        assert e.tolist() == [int(x <= tau) for x in a["gap_hat"].max(axis=1)]
+
 def test_active_flops_formula_matches_enumeration(oracle_mod):
     wl = WORKLOADS["small"]
     row_ptr, col_idx = oracle_mod.plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
