@@ -45,6 +45,7 @@ def parse():
     ap.add_argument("--impl", choices=["fsa", "reference"], default="fsa")
     ap.add_argument("--mode", choices=["norm_bound", "online_max"], default="norm_bound")
     ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--center-keys", action="store_true", help="mean-centred key norms in the bound")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the online-max comparison and gap stats")
@@ -247,7 +248,8 @@ def reference_arm(args, rank):
 
 
 def sweep(args):
-    """Every workload in both softmax modes, one JSON line each (not the bench contract line)."""
+    """Every workload in both softmax modes, and in norm_bound mode once more with mean-centred
+    keys; one JSON line each (not the bench contract line)."""
     import torch
 
     import frame_aligned_block_fsa_b300 as fsa
@@ -258,9 +260,15 @@ def sweep(args):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream()
     peaks, _ = load_peaks()
-    for name in ("tiny", "small", "sr28k", "sr57k", "stress"):
+    cached = {}  # the current workload's device inputs, shared by its two centring settings
+    for name, center in [(n, c) for n in ("tiny", "small", "sr28k", "sr57k", "stress", "offset")
+                         for c in (False, True)]:
         wl = WORKLOADS[name]
-        q, k, v = (t.to(dev) for t in make_workload_inputs(wl))
+        if cached.get("name") != name:
+            cached.clear()
+            torch.cuda.empty_cache()
+            cached.update(name=name, qkv=tuple(t.to(dev) for t in make_workload_inputs(wl)))
+        q, k, v = cached["qkv"]
         H, N, D = wl.H, wl.N, wl.D
         out = torch.empty((H, N, D), dtype=torch.float32, device=dev)
         lse = torch.empty((H, N), dtype=torch.float32, device=dev)
@@ -268,6 +276,7 @@ def sweep(args):
         elig = torch.empty(H, dtype=torch.uint8, device=dev)
         rm = torch.empty((H, N), dtype=torch.float32, device=dev)
         plan = fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
+        plan.set_center_keys(center)
         flops = plan.nnz() * 4 * wl.block * wl.block * D * H
         reps = max(3, min(args.steps, 20))
 
@@ -290,14 +299,15 @@ def sweep(args):
         gap = (bound - rm).flatten()
         qs = torch.quantile(gap[torch.randperm(gap.numel(), device=dev)[:1 << 20]],
                             torch.tensor([0.5, 0.99], device=dev))
-        for mode in ("norm_bound", "online_max"):
+        for mode in ("norm_bound",) if center else ("norm_bound", "online_max"):
             st = fsa.new_stats(dev)
             fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound, eligible=elig, stats=st)
             torch.cuda.synchronize()
             stats = fsa.read_stats(st)
             ms = timed(lambda: fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound, eligible=elig,
                                               stream=stream))
-            line = {"sweep": name, "mode": mode, "workload": workload_desc(wl), "attention_ms": ms,
+            line = {"sweep": name, "mode": mode, "center_keys": center, "workload": workload_desc(wl),
+                    "attention_ms": ms,
                     "attention_tflops": flops / (ms * 1e-3) / 1e12,
                     "frac_of_bf16_peak": flops / (ms * 1e-3) / 1e12 / float(peaks["bf16_tflops"]),
                     "norms_ms": norms_ms, "active_flops": flops, "eligible_heads": int(elig.sum().item()),
@@ -351,6 +361,7 @@ def main():
     bound = torch.empty((H, N), dtype=torch.float32, device=dev)
     elig = torch.empty(H, dtype=torch.uint8, device=dev)
     plan = fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
+    plan.set_center_keys(args.center_keys)
     # active FLOPs: every active (query block, key block) pair does QK^T and PV, 2 * 2 B^2 D each
     flops_step = plan.nnz() * 4 * wl.block * wl.block * D * H
     stream = torch.cuda.current_stream()
@@ -465,13 +476,15 @@ def main():
     attn_avg = sum(attn_ms) / len(attn_ms)
     achieved = flops_step / (attn_avg * 1e-3) / 1e12
     peak = float(peaks["bf16_tflops"])
-    norms_bytes = 2 * H * N * D * 2 + 4 * H * N + 4 * H * wl.F * (D + 1) + H
+    # Q and K read once, bound written, per-frame key statistics; centring reads K once more
+    norms_bytes = (3 if args.center_keys else 2) * H * N * D * 2 + 4 * H * N + 4 * H * wl.F * (D + 1) + H
     norms_avg = sum(norms_ms) / len(norms_ms)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": workload_desc(wl), "mode": args.mode, "step": "fsa_norms + attention, all heads",
+        "config": {"workload": workload_desc(wl), "mode": args.mode, "center_keys": args.center_keys,
+                   "step": "fsa_norms + attention, all heads",
                    "l2": f"inputs {3 * H * N * D * 2 / 1e6:.0f} MB > 126 MB L2, no flush",
                    "active_flops_per_step": flops_step, "parallelism": f"independent batch per rank x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -484,7 +497,8 @@ def main():
                            "frac": norms_bytes / (norms_avg * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
                            "ms_avg": norms_avg, "algorithmic_bytes": norms_bytes},
         "clocks": clk,
-        "gpu_launches": 4 * args.steps,  # per step: 3 norm kernels + the attention kernel
+        # per step: 3 norm kernels (4 with centred keys) + the attention kernel
+        "gpu_launches": (5 if args.center_keys else 4) * args.steps,
         "e2e": e2e,
     }
     line.update(extras)

@@ -27,6 +27,7 @@ FSA_ERR_SCRATCH_LIMIT = -5
 
 # Exported symbols, in the order include/fsa.h declares them.
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
+           "fsa_plan_set_center_keys",
            "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_norms_noalloc",
            "fsa_status_string", "fsa_selftest_wait_timeout")
 
@@ -60,6 +61,8 @@ def load():
             lib.fsa_plan_set_tau.restype = i32
             lib.fsa_plan_set_key_tile.argtypes = [vp, i32]
             lib.fsa_plan_set_key_tile.restype = i32
+            lib.fsa_plan_set_center_keys.argtypes = [vp, i32]
+            lib.fsa_plan_set_center_keys.restype = i32
             lib.fsa_norms.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.fsa_norms.restype = i32
             lib.fsa_forward.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp]
@@ -156,6 +159,9 @@ class Plan:
 
     def set_key_tile(self, key_tile: int):
         _check("fsa_plan_set_key_tile", load().fsa_plan_set_key_tile(self.handle, int(key_tile)))
+
+    def set_center_keys(self, on: bool):
+        _check("fsa_plan_set_center_keys", load().fsa_plan_set_center_keys(self.handle, int(on)))
 
 
 def _check_qkv(plan: Plan, *ts):

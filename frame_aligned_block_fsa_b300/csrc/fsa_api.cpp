@@ -28,6 +28,7 @@ struct fsa_plan_s {
     int n_items = 0;
     float tau = 64.0f;
     int key_tile = 0;                       // 0 = automatic
+    int center_keys = 0;                    // 1: mean-centred key norms in the bound
     std::mutex mu;
     // device data, created on first device use
     int device = -1;
@@ -35,11 +36,13 @@ struct fsa_plan_s {
     int32_t* d_items = nullptr;
     // norms workspace, grown on demand (capacities in elements)
     int64_t cap_qnorm = 0, cap_bound = 0, cap_kmax = 0, cap_ksum = 0, cap_gmax = 0, cap_elig = 0;
-    int64_t cap_psum = 0, cap_pmax = 0, cap_tickets = 0;
+    int64_t cap_psum = 0, cap_pmax = 0, cap_tickets = 0, cap_mu = 0, cap_htickets = 0;
     float* d_psum = nullptr;
     float* d_pmax = nullptr;
     unsigned* d_tickets = nullptr;
     bool tickets_fresh = false;  // newly allocated: zero them on the next norms launch
+    float* d_mu = nullptr;       // [H][D] head key means (centred keys)
+    unsigned* d_htickets = nullptr;
     float* d_qnorm = nullptr;
     float* d_bound = nullptr;
     float* d_kmax = nullptr;
@@ -129,9 +132,11 @@ int ensure_workspace(fsa_plan_s* P, int H, int D)
     const int64_t chunks = fsa::norms_key_chunks(P->T);
     if ((rc = grow(&P->d_psum, &P->cap_psum, hf * chunks * D)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_pmax, &P->cap_pmax, hf * chunks)) != FSA_OK) return rc;
-    const int64_t had = P->cap_tickets;
+    const int64_t had = P->cap_tickets, had_h = P->cap_htickets;
     if ((rc = grow(&P->d_tickets, &P->cap_tickets, hf)) != FSA_OK) return rc;
-    if (P->cap_tickets != had) P->tickets_fresh = true;
+    if ((rc = grow(&P->d_htickets, &P->cap_htickets, static_cast<int64_t>(H))) != FSA_OK) return rc;
+    if (P->cap_tickets != had || P->cap_htickets != had_h) P->tickets_fresh = true;
+    if ((rc = grow(&P->d_mu, &P->cap_mu, static_cast<int64_t>(H) * D)) != FSA_OK) return rc;
     return grow(&P->d_elig, &P->cap_elig, static_cast<int64_t>(H));
 }
 
@@ -195,10 +200,15 @@ int run_norms(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, int H, int D,
     L.tickets = P->d_tickets;
     if (P->tickets_fresh) {
         if (cudaMemsetAsync(P->d_tickets, 0, static_cast<size_t>(P->cap_tickets) * sizeof(unsigned), stream) !=
-            cudaSuccess)
+                cudaSuccess ||
+            cudaMemsetAsync(P->d_htickets, 0, static_cast<size_t>(P->cap_htickets) * sizeof(unsigned), stream) !=
+                cudaSuccess)
             return FSA_ERR_CUDA;
         P->tickets_fresh = false;
     }
+    L.center = P->center_keys;
+    L.mu = P->d_mu;
+    L.htickets = P->d_htickets;
     L.bound = bound ? bound : P->d_bound;
     L.gmax = P->d_gmax;
     L.eligible = eligible ? eligible : P->d_elig;
@@ -289,6 +299,7 @@ int fsa::plan_view(const fsa_plan_s* P, PlanView* out)
     out->T = P->T;
     out->N = P->N;
     out->tau = P->tau;
+    out->center_keys = P->center_keys;
     out->runs = P->runs.data();
     return FSA_OK;
 }
@@ -434,6 +445,8 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_psum);
         cudaFree(plan->d_pmax);
         cudaFree(plan->d_tickets);
+        cudaFree(plan->d_htickets);
+        cudaFree(plan->d_mu);
         cudaFree(plan->d_elig);
         cudaFree(plan->d_hq);
         cudaFree(plan->d_hk);
@@ -462,6 +475,13 @@ int fsa_plan_set_tau(fsa_plan_t plan, float tau)
 {
     if (!plan || !(tau > 0.0f)) return FSA_ERR_INVALID_ARG;
     plan->tau = tau;
+    return FSA_OK;
+}
+
+int fsa_plan_set_center_keys(fsa_plan_t plan, int on)
+{
+    if (!plan || (on != 0 && on != 1)) return FSA_ERR_INVALID_ARG;
+    plan->center_keys = on;
     return FSA_OK;
 }
 

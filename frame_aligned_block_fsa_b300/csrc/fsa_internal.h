@@ -64,6 +64,9 @@ struct NormsLaunch {
     float* bound;          // [H][N]
     unsigned* gmax;        // [H] workspace
     uint8_t* eligible;     // [H]
+    int center;            // 1: key norms about the head's mean key, c <q, mu> added to the bound
+    float* mu;             // [H][D] workspace (center only)
+    unsigned* htickets;    // [H] workspace, zero between launches (center only)
     cudaStream_t stream;
 };
 
@@ -77,6 +80,7 @@ struct PlanView {
     int F, T;
     int64_t N;
     float tau;
+    int center_keys;
     const int32_t* runs;  // host [F][kRunStride]
 };
 

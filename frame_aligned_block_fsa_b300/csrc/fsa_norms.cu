@@ -15,7 +15,13 @@
 //   2. query_bounds      per (row chunk, frame, head): ||q||, bound = c ||q|| Kmax_S, and the
 //                        gap bound c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head;
 //   3. eligibility       per head: max gap bound <= tau.
-// All reductions run in a fixed order, so the results are deterministic.
+// With mean-centred keys (same section: keys share a large common component; subtracting
+// their mean tightens the bound and the softmax does not see it) the last frame of a head to
+// finish also forms the head's key mean mu from the frame sums, a second pass over K
+// (key_centred_max) takes max ||k - mu|| per frame, and query_bounds uses
+// c (||q|| Kmax_S + <q, mu>): Cauchy-Schwarz on the centred logit with the row constant
+// c <q, mu> added back, so it bounds the uncentred logits and the lse needs no correction.
+// All reductions run in a fixed order (or take a max), so the results are deterministic.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -104,7 +110,8 @@ template <int D>
 __global__ void __launch_bounds__(kNormThreads) key_frame_stats_kernel(
     const uint16_t* __restrict__ k, int N, int T, int F, int chunks, int rows_per_chunk,
     float* __restrict__ part_max, float* __restrict__ part_sum, unsigned* __restrict__ tickets,
-    float* __restrict__ kmax, float* __restrict__ ksum, unsigned* __restrict__ gmax)
+    float* __restrict__ kmax, float* __restrict__ ksum, unsigned* __restrict__ gmax, int center,
+    float* __restrict__ mu, unsigned* __restrict__ htickets)
 {
     constexpr int TPR = D / 16;                // threads per row, 16 values each
     constexpr int RPI = kNormThreads / TPR;    // rows per block iteration
@@ -184,16 +191,90 @@ __global__ void __launch_bounds__(kNormThreads) key_frame_stats_kernel(
     if (threadIdx.x == 0) {
         float m = 0.0f;
         for (int i = 0; i < chunks; ++i) m = fmaxf(m, __ldcg(part_max + hg * chunks + i));
-        kmax[hg] = m;
+        // centred: zero here, max-reduced by key_centred_max in the next launch
+        kmax[hg] = center ? 0.0f : m;
         tickets[hg] = 0u;  // ready for the next launch
+    }
+    if (!center) return;
+    // The last frame of this head to finish forms the head's key mean, in frame order.
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const unsigned ticket = atomicAdd(htickets + h, 1u);
+        last = ticket == static_cast<unsigned>(F - 1);
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    if (threadIdx.x < D) {
+        float s = 0.0f;
+        for (int gg = 0; gg < F; ++gg) s += __ldcg(ksum + (static_cast<int64_t>(h) * F + gg) * D + threadIdx.x);
+        mu[static_cast<int64_t>(h) * D + threadIdx.x] = s / static_cast<float>(N);
+    }
+    if (threadIdx.x == 0) htickets[h] = 0u;
+}
+
+// Max over a chunk of a frame's keys of ||k - mu_h||, max-reduced into kmax[h][g] (zeroed by
+// key_frame_stats; non-negative floats order like their bit patterns).
+template <int D>
+__global__ void __launch_bounds__(kNormThreads) key_centred_max_kernel(
+    const uint16_t* __restrict__ k, int N, int T, int F, int rows_per_chunk, const float* __restrict__ mu,
+    float* __restrict__ kmax)
+{
+    constexpr int TPR = D / 16;
+    constexpr int RPI = kNormThreads / TPR;
+    __shared__ float wmax[kNormThreads / 32];
+    const int c = blockIdx.x, g = blockIdx.y, h = blockIdx.z;
+    const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
+    const int r0 = c * rows_per_chunk;
+    const int r1 = min(T, r0 + rows_per_chunk);
+    const uint4* base = reinterpret_cast<const uint4*>(k + (static_cast<int64_t>(h) * N + static_cast<int64_t>(g) * T) * D);
+    float2 nmu[8];  // minus the mean, at this thread's 16 columns
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int col = (i < 4 ? 8 * sub + 2 * i : D / 2 + 8 * sub + 2 * (i - 4));
+        nmu[i] = make_float2(-mu[static_cast<int64_t>(h) * D + col], -mu[static_cast<int64_t>(h) * D + col + 1]);
+    }
+    float mx = 0.0f;
+    for (int rb = r0; rb < r1; rb += kBatch * RPI) {
+        uint4 ua[kBatch], ub[kBatch];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int r = rb + b * RPI + rsel;
+            load_row16<D>(base + static_cast<int64_t>(r) * (D / 8), sub, r < r1, ua[b], ub[b]);
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const bool act = rb + b * RPI + rsel < r1;
+            float2 x[8];
+            unpack16(ua[b], ub[b], x);
+            float2 ss = make_float2(0.0f, 0.0f);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float2 d = add2(x[i], nmu[i]);
+                ss = fma2(d, d, ss);
+            }
+            const float n2 = group_sum<TPR>(ss.x + ss.y);
+            // an inactive row reads zeros, whose distance to the mean is no key's
+            if (act) mx = fmaxf(mx, sqrtf(n2));
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = wmax[0];
+        for (int w = 1; w < kNormThreads / 32; ++w) m = fmaxf(m, wmax[w]);
+        atomicMax(reinterpret_cast<unsigned*>(kmax) + static_cast<int64_t>(h) * F + g, __float_as_uint(m));
     }
 }
 
-template <int D>
+template <int D, bool CENTER>
 __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
     const uint16_t* __restrict__ q, int N, int T, int F, const int32_t* __restrict__ runs, float scale,
-    const float* __restrict__ kmax, const float* __restrict__ ksum, float* __restrict__ qnorm,
-    float* __restrict__ bound, unsigned* __restrict__ gmax, int rows_per_block)
+    const float* __restrict__ kmax, const float* __restrict__ ksum, const float* __restrict__ mu,
+    float* __restrict__ qnorm, float* __restrict__ bound, unsigned* __restrict__ gmax, int rows_per_block)
 {
     constexpr int TPR = D / 16;
     constexpr int RPI = kNormThreads / TPR;
@@ -241,11 +322,12 @@ __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
     }
     __syncthreads();
     const float K = kh_s;
-    float2 kb[8];
+    float2 kb[8], mb[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int col = (i < 4 ? 8 * sub + 2 * i : D / 2 + 8 * sub + 2 * (i - 4));
         kb[i] = make_float2(kbar[col], kbar[col + 1]);
+        if (CENTER) mb[i] = make_float2(mu[static_cast<int64_t>(h) * D + col], mu[static_cast<int64_t>(h) * D + col + 1]);
     }
     float gworst = 0.0f;
     for (int rb = r0; rb < r1; rb += kBatch * RPI) {
@@ -262,16 +344,18 @@ __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
             const bool act = r < r1;
             float2 x[8];
             unpack16(ua[b], ub[b], x);
-            float2 ss = make_float2(0.0f, 0.0f), dot = make_float2(0.0f, 0.0f);
+            float2 ss = make_float2(0.0f, 0.0f), dot = make_float2(0.0f, 0.0f), qm = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 ss = fma2(x[i], x[i], ss);
                 dot = fma2(x[i], kb[i], dot);
+                if (CENTER) qm = fma2(x[i], mb[i], qm);
             }
             const float n2 = group_sum<TPR>(ss.x + ss.y);
             const float dt = group_sum<TPR>(dot.x + dot.y);
             const float qn = sqrtf(n2);
-            const float qk = qn * K;
+            // the bound before the factor c: ||q|| Kmax_S, centred ||q|| Kmax_S + <q, mu>
+            const float qk = CENTER ? fmaf(qn, K, group_sum<TPR>(qm.x + qm.y)) : qn * K;
             if (act) gworst = fmaxf(gworst, scale * (qk - dt));
             if (act && sub == 0) {
                 if (qnorm) qnorm[row_base + r] = qn;
@@ -310,13 +394,21 @@ static int launch_norms_d(const NormsLaunch& L)
     const int chunks = norms_key_chunks(L.T);
     const int rows_per_chunk = (L.T + chunks - 1) / chunks;
     key_frame_stats_kernel<D><<<dim3(chunks, L.F, L.H), kNormThreads, 0, L.stream>>>(
-        L.k, L.N, L.T, L.F, chunks, rows_per_chunk, L.part_max, L.part_sum, L.tickets, L.kmax, L.ksum, L.gmax);
+        L.k, L.N, L.T, L.F, chunks, rows_per_chunk, L.part_max, L.part_sum, L.tickets, L.kmax, L.ksum, L.gmax,
+        L.center, L.mu, L.htickets);
+    if (L.center)
+        key_centred_max_kernel<D><<<dim3(chunks, L.F, L.H), kNormThreads, 0, L.stream>>>(L.k, L.N, L.T, L.F,
+                                                                                         rows_per_chunk, L.mu, L.kmax);
     // about 256 query rows per block, split evenly over a frame (T = 1200: 5 blocks of 240)
     const int qblocks = (L.T + 255) / 256;
     const int rows_per_block = (L.T + qblocks - 1) / qblocks;
     const dim3 grid(qblocks, L.F, L.H);
-    query_bounds_kernel<D><<<grid, kNormThreads, 0, L.stream>>>(L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum,
-                                                                L.qnorm, L.bound, L.gmax, rows_per_block);
+    if (L.center)
+        query_bounds_kernel<D, true><<<grid, kNormThreads, 0, L.stream>>>(
+            L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum, L.mu, L.qnorm, L.bound, L.gmax, rows_per_block);
+    else
+        query_bounds_kernel<D, false><<<grid, kNormThreads, 0, L.stream>>>(
+            L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum, nullptr, L.qnorm, L.bound, L.gmax, rows_per_block);
     eligibility_kernel<<<(L.H + 127) / 128, 128, 0, L.stream>>>(L.gmax, L.tau, L.eligible, L.H);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }

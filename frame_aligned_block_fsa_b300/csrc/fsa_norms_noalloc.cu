@@ -68,18 +68,20 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     if (!q || !k || !kmax || !bound || !eligible) return FSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return FSA_ERR_INVALID_ARG;
 
-    // scratch layout: per-frame tickets | key runs of every query frame | per-frame key sums |
-    // per-chunk key sums | per-chunk max key norms | per-head gap maxima
+    // scratch layout: per-frame and per-head tickets | key runs of every query frame | per-frame
+    // key sums | per-chunk key sums | per-chunk max key norms | per-head gap maxima | per-head
+    // key means (used with centred keys)
     const size_t hf = static_cast<size_t>(H) * pv.F;
     const size_t chunks = static_cast<size_t>(fsa::norms_key_chunks(pv.T));
-    const size_t tickets_bytes = hf * sizeof(unsigned);
+    const size_t tickets_bytes = (hf + static_cast<size_t>(H)) * sizeof(unsigned);
     const size_t runs_bytes = static_cast<size_t>(pv.F) * fsa::kRunStride * sizeof(int32_t);
     const size_t off_runs = fsa::round256(tickets_bytes);
     const size_t off_ksum = off_runs + fsa::round256(runs_bytes);
     const size_t off_psum = off_ksum + fsa::round256(hf * D * sizeof(float));
     const size_t off_pmax = off_psum + fsa::round256(hf * chunks * D * sizeof(float));
     const size_t off_gmax = off_pmax + fsa::round256(hf * chunks * sizeof(float));
-    const size_t total = off_gmax + fsa::round256(static_cast<size_t>(H) * sizeof(unsigned));
+    const size_t off_mu = off_gmax + fsa::round256(static_cast<size_t>(H) * sizeof(unsigned));
+    const size_t total = off_mu + fsa::round256(static_cast<size_t>(H) * D * sizeof(float));
     if (total > fsa::kNoAllocScratchBytes) return FSA_ERR_SCRATCH_LIMIT;
 
     void* base = nullptr;
@@ -114,6 +116,9 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     L.bound = bound;
     L.gmax = reinterpret_cast<unsigned*>(s + off_gmax);
     L.eligible = eligible;
+    L.center = pv.center_keys;
+    L.mu = reinterpret_cast<float*>(s + off_mu);
+    L.htickets = reinterpret_cast<unsigned*>(s) + hf;
     L.stream = st;
     rc = fsa::launch_norms(L);
     return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);

@@ -8,8 +8,10 @@ Recipes (the pages measure on production data, which is not available):
           scalar (per head, per token); in each head ceil(0.001 N) key tokens,
           chosen uniformly without replacement, are further scaled by 8;
           V is N(0, 1).
+  offset: as normal, then one vector m_h ~ N(0, 4^2 I_D) per head is added to every key
+          of head h (a large component that all keys share).
 All draws come from one CPU torch.Generator seeded with the workload's seed, in
-the order q, k, v (then the stress scalars and outlier choice), so a seed fixes
+the order q, k, v (then the stress scalars and outlier choice, or the key offsets), so a seed fixes
 the inputs on every machine.
 """
 from __future__ import annotations
@@ -19,6 +21,9 @@ import math
 import torch
 
 from .workloads import Workload
+
+
+KEY_OFFSET_STD = 4.0  # spread of the shared key component of the "offset" inputs
 
 
 def make_qkv(H: int, N: int, D: int, seed: int, kind: str = "normal"):
@@ -37,6 +42,9 @@ def make_qkv(H: int, N: int, D: int, seed: int, kind: str = "normal"):
         for h in range(H):
             idx = torch.randperm(N, generator=g)[:n_out]
             k[h, idx, :] *= 8.0
+    elif kind == "offset":
+        m = torch.randn((H, 1, D), generator=g, dtype=torch.float32).mul_(KEY_OFFSET_STD)
+        k.add_(m)
     elif kind != "normal":
         raise ValueError(f"unknown input kind {kind!r}")
     return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),

@@ -20,7 +20,8 @@ class Workload:
     w: int          # window half-width in frames
     ref: int        # global reference frame
     block: int      # plan block size: a multiple of 16 dividing T
-    kind: str       # "normal" (i.i.d. N(0,1)) or "stress" (log-normal row norms + outlier keys)
+    kind: str       # "normal" (i.i.d. N(0,1)), "stress" (log-normal row norms + outlier keys) or
+                    # "offset" (keys share one large per-head component)
     seed: int
 
     @property
@@ -38,6 +39,8 @@ WORKLOADS = {
     # inputs (177 MB) still exceed L2, and the whole case holds ~0.3 GB on the device, which keeps
     # a many-pass profiler capture small.
     "sr28k_h8": Workload("sr28k_h8", F=24, T=1200, H=8, D=128, w=2, ref=0, block=80, kind="normal", seed=5),
+    # sr28k shapes with a shared key component: the case mean-centred keys are for
+    "offset": Workload("offset", F=24, T=1200, H=24, D=128, w=2, ref=0, block=80, kind="offset", seed=6),
 }
 
 # The 28.8k-token workload is the one the throughput target is stated on.

@@ -115,6 +115,21 @@ int fsa_plan_set_tau(fsa_plan_t plan, float tau);
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
 
 /*
+ * fsa_plan_set_center_keys -- mean-centred key norms in the bound (on = 1) or not (0, the
+ * default).  Source: aihot.vn page above, "Giai phong Softmax": keys share a large common
+ * component, so measuring their norms about the key mean tightens the bound, and the
+ * softmax is invariant to the shift.  With on = 1, per head h
+ *     mu_h         = mean of all N keys of head h
+ *     kmax[h][g]   = max over keys n of frame g of ||k_{h,n} - mu_h||
+ *     bound[h][n]  = c * (qnorm[h][n] * max_{g in S(frame(n))} kmax[h][g] + <q_{h,n}, mu_h>)
+ * and the eligibility statistic is bound - c <q_i, kbar_S(f)> as without centring.  The
+ * bound is still an upper bound on the uncentred logits, so out and lse mean the same in
+ * both settings.  It costs a second read of K in fsa_norms / fsa_norms_noalloc.
+ * Errors: FSA_ERR_INVALID_ARG for a NULL plan or on not in {0, 1}.
+ */
+int fsa_plan_set_center_keys(fsa_plan_t plan, int on);
+
+/*
  * fsa_norms -- the precomputed norm arrays of the bound.
  * Source: aihot.vn page above, section "Giai phong Softmax": by Cauchy-Schwarz the
  * largest logit of a query is at most its norm times the largest key norm; a small
@@ -122,6 +137,7 @@ int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
  *   qnorm[h][n]  = ||q_{h,n}||                                (fp32 sum of bf16 squares)
  *   kmax[h][g]   = max over keys n of frame g of ||k_{h,n}||
  *   bound[h][n]  = c * qnorm[h][n] * max_{g in S(frame(n))} kmax[h][g]
+ *   (kmax and bound take their centred forms when fsa_plan_set_center_keys is on)
  *   eligible[h]  = 1 iff the head passes the tau test of fsa_plan_set_tau
  * q, k: device bf16 [H][N][D].  Any output pointer may be NULL (the value is then kept
  * only in the plan's workspace).  Uses plan-owned workspace (per-frame key sums).
@@ -199,9 +215,9 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
  * `stream`).
  *   Arguments and results are those of fsa_norms, except that kmax, bound and eligible are
  *   required (they are the outputs; qnorm may be NULL).
- *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, H*F*4 + F*9*4 + H*F*D*4 +
- *   H*F*C*D*4 + H*F*C*4 + H*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
- *   H=24, F=24, T=1200, D=128 uses 1.5 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT
+ *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, (H*F + H)*4 + F*9*4 + H*F*D*4 +
+ *   H*F*C*D*4 + H*F*C*4 + H*4 + H*D*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
+ *   H=24, F=24, T=1200, D=128 uses 1.4 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT
  *   before any device work.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
  *   with that device current; make that first call before any stream capture.

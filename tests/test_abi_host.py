@@ -93,6 +93,11 @@ def test_plan_setters_validate(lib):
             assert lib.fsa_plan_set_key_tile(p.handle, bad) == fsa.FSA_ERR_INVALID_ARG, bad
         for good in (0, 16, 48, 64, 80, 112, 128):
             assert lib.fsa_plan_set_key_tile(p.handle, good) == fsa.FSA_OK
+        for bad in (-1, 2, 7):
+            assert lib.fsa_plan_set_center_keys(p.handle, bad) == fsa.FSA_ERR_INVALID_ARG, bad
+        for good in (1, 0):
+            assert lib.fsa_plan_set_center_keys(p.handle, good) == fsa.FSA_OK
+    assert lib.fsa_plan_set_center_keys(None, 1) == fsa.FSA_ERR_INVALID_ARG
 
 
 def test_forward_rejects_bad_arguments_before_device_work(lib):

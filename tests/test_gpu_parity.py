@@ -61,12 +61,15 @@ def _oracle_sampled(oracle_mod, name, per_head):
     return _cache[key]
 
 
-def _gpu(dev, q, k, v, F, T, w, ref, block, mode, key_tile=0, tau=None, rowmax=False, stats=False):
+def _gpu(dev, q, k, v, F, T, w, ref, block, mode, key_tile=0, tau=None, rowmax=False, stats=False,
+         center_keys=False):
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     H, N, D = q.shape
     with fsa.Plan(F, T, w, ref, block) as plan:
         if key_tile:
             plan.set_key_tile(key_tile)
+        if center_keys:
+            plan.set_center_keys(True)
         if tau is not None:
             plan.set_tau(tau)
         rm = torch.full((H, N), float("nan"), device=dev) if rowmax else None
@@ -299,6 +302,93 @@ def test_bound_dominates_row_max_on_gpu(dev):
         torch.cuda.synchronize()
     b, m = bd.cpu().double().numpy(), rm.cpu().double().numpy()
     assert np.all(b >= m - 1e-5 * np.abs(b))
+
+
+# ------------------------------------------------------------------- mean-centred keys
+def _gpu_norms(dev, q, k, wl, center_keys, noalloc=False):
+    H, N, D = q.shape
+    qd, kd = q.to(dev), k.to(dev)
+    qn = torch.full((H, N), -1.0, device=dev)
+    km = torch.full((H, wl.F), -1.0, device=dev)
+    bd = torch.full((H, N), -1.0, device=dev)
+    el = torch.full((H,), 7, dtype=torch.uint8, device=dev)
+    with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+        plan.set_center_keys(center_keys)
+        fsa.norms(qd, kd, plan, qn, km, bd, el)
+        torch.cuda.synchronize()
+    return {"qnorm": qn.cpu().double().numpy(), "kmax": km.cpu().double().numpy(),
+            "bound": bd.cpu().double().numpy(), "eligible": el.cpu().numpy()}
+
+
+@pytest.mark.parametrize("name", ["tiny", "small", "offset"])
+def test_centred_norms_parity(dev, oracle_mod, name):
+    wl = WORKLOADS[name]
+    q, k, _ = _inputs(name)
+    H, N, D = q.shape
+    on = oracle_mod.norms(q, k, wl.F, wl.T, wl.w, wl.ref, center=True)
+    got = _gpu_norms(dev, q, k, wl, True)
+    np.testing.assert_allclose(got["qnorm"], on["qnorm"], rtol=2e-6)
+    # fp32 centring: k - mu and <q, mu> carry errors of order 2^-24 times the key and mean
+    # magnitudes; the tolerance scales with c ||q|| (Kc + ||mu||)
+    mu_norm = np.linalg.norm(k.double().numpy().mean(axis=1), axis=-1)  # [H], a tolerance scale only
+    np.testing.assert_allclose(got["kmax"], on["kmax"], rtol=2e-5, atol=0)
+    c = 1.0 / math.sqrt(D)
+    scale = c * on["qnorm"] * (on["kmax"].max(axis=1) + mu_norm)[:, None]
+    assert np.all(np.abs(got["bound"] - on["bound"]) <= 2e-5 * scale + 1e-6)
+    worst = on["gap_hat"].max(axis=1)
+    margin = np.abs(worst - oracle_mod.DEFAULT_TAU) > 1e-3 * oracle_mod.DEFAULT_TAU
+    assert np.array_equal(got["eligible"][margin], on["eligible"][margin])
+
+
+def test_centred_keys_make_offset_heads_eligible(dev, oracle_mod):
+    # Keys that share a large per-head component: without centring most heads fail the gap
+    # test and run with the running max; with centring every head takes the fixed bound.  The
+    # outputs are the same attention either way (sampled rows against the oracle).
+    name = "offset"
+    wl = WORKLOADS[name]
+    q, k, v = _inputs(name)
+    heads, rows, ref = _oracle_sampled(oracle_mod, name, per_head=16)
+    for center, in ((False,), (True,)):
+        on = oracle_mod.norms(q, k, wl.F, wl.T, wl.w, wl.ref, center=center)
+        res = _gpu(dev, q, k, v, wl.F, wl.T, wl.w, wl.ref, wl.block, "norm_bound", stats=True,
+                   center_keys=center)
+        assert res["stats"]["fallback_heads"] == int((on["eligible"] == 0).sum())
+        assert res["stats"]["underflow_rows"] == 0
+        _check(res["out"][heads, rows], res["lse"][heads, rows], ref["out"], ref["lse"])
+        if center:
+            assert res["stats"]["fallback_heads"] == 0
+        else:
+            assert res["stats"]["fallback_heads"] >= wl.H // 2
+
+
+def test_centred_bound_dominates_row_max_on_gpu(dev):
+    wl = WORKLOADS["small"]
+    q, k, v = make_qkv(wl.H, wl.N, wl.D, seed=41, kind="offset")
+    H, N, D = q.shape
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+        plan.set_center_keys(True)
+        bd = torch.empty((H, N), device=dev)
+        el = torch.empty(H, dtype=torch.uint8, device=dev)
+        fsa.norms(qd, kd, plan, None, None, bd, el)
+        rm = torch.empty((H, N), device=dev)
+        fsa.forward_ex(qd, kd, vd, plan, "online_max", bound=bd, eligible=el, rowmax=rm)
+        torch.cuda.synchronize()
+    b, m = bd.cpu().double().numpy(), rm.cpu().double().numpy()
+    # the centred bound can sit exactly at the row max, so rounding may put it a few ulps of
+    # the logit magnitude below
+    mag = np.abs(m) + np.abs(b) + 1.0
+    assert np.all(b >= m - 1e-5 * mag)
+
+
+@pytest.mark.parametrize("mode", ["norm_bound", "online_max"])
+def test_centred_forward_full_parity(dev, oracle_mod, mode):
+    H, F, T, D, w, ref, block = 2, 6, 128, 128, 1, 0, 64
+    q, k, v = make_qkv(H, F * T, D, seed=43, kind="offset")
+    exp = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    res = _gpu(dev, q, k, v, F, T, w, ref, block, mode, stats=True, center_keys=True)
+    _check(res["out"], res["lse"], exp["out"], exp["lse"])
+    assert res["stats"]["fallback_heads"] == 0
 
 
 # ------------------------------------------------------------------------ edge shapes

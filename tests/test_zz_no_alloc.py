@@ -97,3 +97,31 @@ def test_noalloc_rejects_problems_beyond_its_scratch_before_device_work():
         rc = lib.fsa_norms_noalloc(fake, fake, 2, 128, plan.handle, None, None, fake, fake, None)
         assert rc == fsa.FSA_ERR_INVALID_ARG  # kmax is a required output
         assert lib.fsa_norms_noalloc(fake, fake, 0, 128, plan.handle, None, None, None, None, None) == fsa.FSA_OK
+
+
+@pytest.mark.gpu
+def test_noalloc_centred_keys_match_fsa_norms():
+    # mean-centred keys through both entry points, then an uncentred call over the leftovers
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    from frame_aligned_block_fsa_b300 import build
+
+    build.build()
+    fsa.load()
+    dev = torch.device("cuda:0")
+    H, F, T, D, w, ref, block, seed = CASES[0]
+    q, k, _ = make_qkv(H, F * T, D, seed, kind="offset")
+    qd, kd = q.to(dev), k.to(dev)
+    got = {}
+    for center in (True, False):
+        with fsa.Plan(F, T, w, ref, block) as plan:
+            plan.set_center_keys(center)
+            a = _outputs(dev, H, F, F * T)
+            b = _outputs(dev, H, F, F * T)
+            fsa.norms(qd, kd, plan, *a)
+            fsa.norms_noalloc(qd, kd, plan, b[1], b[2], b[3], qnorm=b[0])
+            torch.cuda.synchronize()
+        for name, x, y in zip(("qnorm", "kmax", "bound", "eligible"), a, b):
+            assert torch.equal(x, y), name
+        got[center] = a
+    # the shared key component makes the centred key norms smaller
+    assert bool((got[True][1] < got[False][1]).all())
