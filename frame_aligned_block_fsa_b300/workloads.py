@@ -1,4 +1,4 @@
-"""The five synthetic workloads of frame-structured sparse attention (shapes only).
+"""The synthetic workloads of frame-structured sparse attention (shapes only).
 
 Tokens are F frames x T tokens per frame; each query frame attends the key frames
 within +-w of itself plus the reference frame `ref`.  The pages give no production
