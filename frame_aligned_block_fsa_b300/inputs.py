@@ -10,6 +10,8 @@ Recipes (the pages measure on production data, which is not available):
           V is N(0, 1).
   offset: as normal, then one vector m_h ~ N(0, 4^2 I_D) per head is added to every key
           of head h (a large component that all keys share).
+  prep:   hidden states x ~ N(0, 1) [N][d_model] and projection weights
+          w ~ N(0, 1/d_model) [3 H D][d_model], drawn in that order (make_prep_inputs).
 All draws come from one CPU torch.Generator seeded with the workload's seed, in
 the order q, k, v (then the stress scalars and outlier choice, or the key offsets), so a seed fixes
 the inputs on every machine.
@@ -49,6 +51,17 @@ def make_qkv(H: int, N: int, D: int, seed: int, kind: str = "normal"):
         raise ValueError(f"unknown input kind {kind!r}")
     return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),
             v.to(torch.bfloat16).contiguous())
+
+
+def make_prep_inputs(N: int, d_model: int, H: int, D: int, seed: int):
+    """Hidden states x ~ N(0, 1) [N][d_model] and projection weights w ~ N(0, 1/d_model)
+    [3 H D][d_model] (q, k, v rows, head-major), both bf16 on the CPU; with unit-RMS rows after
+    the normalisation, q, k and v come out about N(0, 1)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+    x = torch.randn((N, d_model), generator=g, dtype=torch.float32)
+    w = torch.randn((3 * H * D, d_model), generator=g, dtype=torch.float32).mul_(1.0 / math.sqrt(d_model))
+    return x.to(torch.bfloat16).contiguous(), w.to(torch.bfloat16).contiguous()
 
 
 def make_workload_inputs(wl: Workload):

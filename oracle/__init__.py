@@ -67,6 +67,8 @@ def _load():
             lib.oracle_attention_rows.restype = i32
             lib.oracle_norms.argtypes = [vp] * 2 + [i32] * 6 + [dbl, dbl, i32] + [vp] * 5
             lib.oracle_norms.restype = i32
+            lib.oracle_prep_rows.argtypes = [vp, vp, i64] + [i32] * 3 + [dbl, dbl, i64] + [vp] * 4 + [i32]
+            lib.oracle_prep_rows.restype = i32
             _lib = lib
     return _lib
 
@@ -187,6 +189,36 @@ def norms(q, k, F: int, T: int, w: int, ref: int, scale: float | None = None,
     if rc != 0:
         raise ValueError("oracle_norms: bad arguments")
     return res
+
+
+PREP_EPS = 1e-6       # RMS-norm epsilon (the pages give none)
+PREP_ROPE_BASE = 10000.0
+
+
+def prep_rows(x, w, H: int, D: int, rows, eps: float = PREP_EPS, base: float = PREP_ROPE_BASE,
+              nthreads: int | None = None) -> dict:
+    """RMS norm, QKV projection, rotary embedding of q and k, for the listed token rows.
+
+    x: bf16 [N][d_model]; w: bf16 [3 H D][d_model] (q rows, then k, then v, head-major).
+    Returns fp64 q, k, v of shape [R][H][D]."""
+    xb, wb = _bits(x), _bits(w)
+    N, dm = xb.shape
+    assert wb.shape == (3 * H * D, dm)
+    rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+    R = rows.shape[0]
+    res = {name: np.zeros((R, H, D)) for name in ("q", "k", "v")}
+    rc = _load().oracle_prep_rows(_ptr(xb), _ptr(wb), N, dm, H, D, float(eps), float(base), R, _ptr(rows),
+                                  _ptr(res["q"]), _ptr(res["k"]), _ptr(res["v"]), nthreads or default_threads())
+    if rc != 0:
+        raise ValueError("oracle_prep_rows: bad arguments")
+    return res
+
+
+def prep_full(x, w, H: int, D: int, eps: float = PREP_EPS, base: float = PREP_ROPE_BASE) -> dict:
+    """Every token row; q, k, v as fp64 [H][N][D] (the attention's layout)."""
+    N = tuple(x.shape)[0]
+    res = prep_rows(x, w, H, D, np.arange(N, dtype=np.int64), eps, base)
+    return {name: np.ascontiguousarray(a.transpose(1, 0, 2)) for name, a in res.items()}
 
 
 def active_flops(F: int, T: int, w: int, ref: int, H: int, D: int) -> int:

@@ -7,8 +7,9 @@
  * and this file shares no code with it.
  *
  * Source of the method: "HeyGen toi uu hoa mo hinh Avatar IV tren Google Cloud
- * Trillium TPU" (aihot.vn), sections "Xoa bo mat na" (the frame mask, Fig. 3)
- * and "Giai phong Softmax" (the norm bound, Fig. 4); the same material is in
+ * Trillium TPU" (aihot.vn), sections "Xoa bo mat na" (the frame mask, Fig. 3),
+ * "Giai phong Softmax" (the norm bound, Fig. 4) and "Bo cuc la ABI" (the fused
+ * preparation of the attention inputs, Fig. 5); the same material is in
  * "HeyGen priskoryla Avatar IV na TPU u 1,86 raza" (bib.com.ua), sections on
  * the sparse-attention mask and the softmax chain.
  *
@@ -406,5 +407,119 @@ int oracle_norms(const uint16_t* q, const uint16_t* k, int H, int F, int T, int 
     }
     free(kbar);
     free(mu);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Pre-attention preparation (aihot.vn page, "Bo cuc la ABI", Fig. 5: the
+ * normalisation, rotary embeddings, projection and head packing that produce
+ * the attention's inputs, fused there into one kernel that writes the layout
+ * the next step reads).  The pages name the steps but not their exact form;
+ * readings of this build:
+ *   normalisation   RMS norm over the model dimension, no learned gain (a gain
+ *                   folds into the projection weights):
+ *                       xhat = x / sqrt(mean_c x_c^2 + eps)
+ *   projection      y = xhat W^T, W bf16 [3 H D][d_model]; rows 0..HD-1 give q
+ *                   (head h at rows hD..hD+D-1), then k, then v; no bias
+ *   rotary          q and k of every head, position = token index n, pairs
+ *                   (i, i + D/2) rotated by the angle n * base^(-2i/D):
+ *                       a' = a cos - b sin,  b' = a sin + b cos
+ *                   v is not rotated
+ *   head packing    q, k, v written as [H][N][D]
+ * Everything in fp64, from the bf16 inputs widened exactly.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    const uint16_t* x;
+    const uint16_t* w;
+    int64_t N;
+    int dm, H, D;
+    double eps, base;
+    const int64_t* rows;
+    double *q, *k, *v;
+    int64_t r0, r1;
+} prep_job;
+
+static void prep_one_row(const prep_job* J, int64_t r, double* xh, double* y)
+{
+    const int dm = J->dm, H = J->H, D = J->D, half = J->D / 2;
+    const int64_t n = J->rows[r];
+    const uint16_t* xr = J->x + n * dm;
+    double ss = 0.0;
+    for (int c = 0; c < dm; ++c) {
+        double a = bf16_to_double(xr[c]);
+        xh[c] = a;
+        ss += a * a;
+    }
+    const double rms = sqrt(ss / (double)dm + J->eps);
+    for (int c = 0; c < dm; ++c) xh[c] /= rms;
+    const int64_t nout = (int64_t)3 * H * D;
+    for (int64_t j = 0; j < nout; ++j) {
+        const uint16_t* wr = J->w + j * dm;
+        double s = 0.0;
+        for (int c = 0; c < dm; ++c) s += xh[c] * bf16_to_double(wr[c]);
+        y[j] = s;
+    }
+    for (int h = 0; h < H; ++h) {
+        double* qo = J->q + (r * H + h) * D;
+        double* ko = J->k + (r * H + h) * D;
+        double* vo = J->v + (r * H + h) * D;
+        const double* yq = y + (int64_t)h * D;
+        const double* yk = y + (int64_t)(H + h) * D;
+        const double* yv = y + (int64_t)(2 * H + h) * D;
+        for (int i = 0; i < half; ++i) {
+            const double theta = pow(J->base, -2.0 * (double)i / (double)D);
+            const double ang = (double)n * theta;
+            const double cs = cos(ang), sn = sin(ang);
+            qo[i] = yq[i] * cs - yq[i + half] * sn;
+            qo[i + half] = yq[i] * sn + yq[i + half] * cs;
+            ko[i] = yk[i] * cs - yk[i + half] * sn;
+            ko[i + half] = yk[i] * sn + yk[i + half] * cs;
+        }
+        for (int d = 0; d < D; ++d) vo[d] = yv[d];
+    }
+}
+
+static void* prep_worker(void* arg)
+{
+    const prep_job* J = (const prep_job*)arg;
+    double* xh = (double*)malloc(sizeof(double) * (size_t)J->dm);
+    double* y = (double*)malloc(sizeof(double) * (size_t)3 * J->H * J->D);
+    if (xh && y)
+        for (int64_t r = J->r0; r < J->r1; ++r) prep_one_row(J, r, xh, y);
+    free(xh);
+    free(y);
+    return NULL;
+}
+
+/*
+ * q, k, v of the listed token rows, all heads: outputs [nrows][H][D] fp64.
+ * x: bf16 [N][dm]; w: bf16 [3 H D][dm].  Returns 0, or -1 on bad arguments.
+ */
+int oracle_prep_rows(const uint16_t* x, const uint16_t* w, int64_t N, int dm, int H, int D,
+                     double eps, double base, int64_t nrows, const int64_t* rows,
+                     double* q, double* k, double* v, int nthreads)
+{
+    if (N <= 0 || dm <= 0 || H <= 0 || D <= 0 || D % 2 != 0 || nrows < 0 || eps < 0.0 || !(base > 0.0))
+        return -1;
+    for (int64_t r = 0; r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return -1;
+    if (nthreads < 1) nthreads = 1;
+    if ((int64_t)nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
+    pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+    prep_job* jobs = (prep_job*)malloc(sizeof(prep_job) * (size_t)nthreads);
+    if (!th || !jobs) {
+        free(th);
+        free(jobs);
+        return -1;
+    }
+    for (int t = 0; t < nthreads; ++t) {
+        prep_job J = {x, w, N, dm, H, D, eps, base, rows, q, k, v,
+                      nrows * t / nthreads, nrows * (t + 1) / nthreads};
+        jobs[t] = J;
+        pthread_create(&th[t], NULL, prep_worker, &jobs[t]);
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    free(th);
+    free(jobs);
     return 0;
 }

@@ -348,6 +348,70 @@ def test_centred_equals_uncentred_for_zero_mean_keys(oracle_mod):
         e = oracle_mod.norms(q, kk, F, T, w, ref, tau=tau, center=True)["eligible"]
         assert e.tolist() == [int(x <= tau) for x in a["gap_hat"].max(axis=1)]
 
+# --------------------------------------------------------------------------- prep
+def test_prep_hand_derived_rotation(oracle_mod):
+    # H = 1, D = 4, d_model = 4, eps = 0, base 100: theta = (1, 1/10).  W = [I; 2I; 3I] (q, k,
+    # v).  Token 1 is x = (2, 0, 0, 2): rms = sqrt(8/4) = sqrt 2, xhat = (sqrt2, 0, 0, sqrt2).
+    # Pairs (0, 2) and (1, 3) turn by 1 and 0.1 rad at position 1:
+    #   q = (s cos1 - 0 sin1, 0 cos.1 - s sin.1, s sin1 + 0 cos1, 0 sin.1 + s cos.1), s = sqrt2
+    # k is 2 q, v = 3 xhat unrotated; token 0 (position 0) is not rotated at all.
+    x = _bf16([[1, -1, 1, -1], [2, 0, 0, 2]])
+    eye = np.eye(4, dtype=np.float32)
+    w = _bf16(np.concatenate([eye, 2 * eye, 3 * eye]))
+    r = oracle_mod.prep_full(x, w, H=1, D=4, eps=0.0, base=100.0)
+    s = math.sqrt(2.0)
+    q1 = [s * math.cos(1.0), -s * math.sin(0.1), s * math.sin(1.0), s * math.cos(0.1)]
+    np.testing.assert_allclose(r["q"][0, 1], q1, atol=1e-15)
+    np.testing.assert_allclose(r["k"][0, 1], 2 * np.asarray(q1), atol=1e-15)
+    np.testing.assert_allclose(r["v"][0, 1], [3 * s, 0, 0, 3 * s], atol=1e-15)
+    np.testing.assert_allclose(r["q"][0, 0], [1, -1, 1, -1], atol=1e-15)  # rms 1, no rotation
+    np.testing.assert_allclose(r["v"][0, 0], [3, -3, 3, -3], atol=1e-15)
+
+
+def _numpy_projection(x, w, eps):
+    xx = _f64(x)
+    xh = xx / np.sqrt((xx * xx).mean(axis=1, keepdims=True) + eps)
+    return xh @ _f64(w).T  # [N][3 H D]
+
+
+def test_prep_projection_norms_and_relative_positions(oracle_mod):
+    from frame_aligned_block_fsa_b300.inputs import make_prep_inputs
+
+    N, dm, H, D = 40, 96, 2, 16
+    x, w = make_prep_inputs(N, dm, H, D, seed=51)
+    # tokens 30..39 repeat tokens 0..9 ten positions later
+    x[30:40] = x[0:10]
+    r = oracle_mod.prep_full(x, w, H, D)
+    y = _numpy_projection(x, w, oracle_mod.PREP_EPS).reshape(N, 3, H, D).transpose(1, 2, 0, 3)
+    # v and every row at position 0 are the plain projection (numpy matmul)
+    np.testing.assert_allclose(r["v"], y[2], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["q"][:, 0], y[0][:, 0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(r["k"][:, 0], y[1][:, 0], rtol=1e-12, atol=1e-12)
+    # the rotation keeps every head row's norm
+    np.testing.assert_allclose(np.linalg.norm(r["q"], axis=-1), np.linalg.norm(y[0], axis=-1), rtol=1e-12)
+    np.testing.assert_allclose(np.linalg.norm(r["k"], axis=-1), np.linalg.norm(y[1], axis=-1), rtol=1e-12)
+    # logits depend on the positions only through their difference
+    a = np.einsum("hmd,hnd->hmn", r["q"][:, 0:10], r["k"][:, 0:10])
+    b = np.einsum("hmd,hnd->hmn", r["q"][:, 30:40], r["k"][:, 30:40])
+    np.testing.assert_allclose(b, a, rtol=1e-9, atol=1e-9)
+    # ... and do change with it (the rotation is not the identity)
+    assert np.abs(r["q"][:, 30] - r["q"][:, 0]).max() > 1e-2
+
+
+def test_prep_rms_norm_scale_invariance_and_row_sampling(oracle_mod):
+    from frame_aligned_block_fsa_b300.inputs import make_prep_inputs
+
+    N, dm, H, D = 24, 64, 2, 8
+    x, w = make_prep_inputs(N, dm, H, D, seed=52)
+    a = oracle_mod.prep_full(x, w, H, D, eps=0.0)
+    b = oracle_mod.prep_full((x.float() * 4).to(torch.bfloat16), w, H, D, eps=0.0)  # exact in bf16
+    for name in ("q", "k", "v"):
+        np.testing.assert_allclose(b[name], a[name], rtol=1e-13, atol=1e-13)
+    rows = np.array([23, 0, 7, 7], dtype=np.int64)
+    s = oracle_mod.prep_rows(x, w, H, D, rows, eps=0.0)
+    for name in ("q", "k", "v"):
+        np.testing.assert_array_equal(s[name], a[name][:, rows].transpose(1, 0, 2))
+
 def test_active_flops_formula_matches_enumeration(oracle_mod):
     wl = WORKLOADS["small"]
     row_ptr, col_idx = oracle_mod.plan(wl.F, wl.T, wl.w, wl.ref, wl.block)
