@@ -7,15 +7,17 @@ Public API (thin wrappers over the C ABI in include/fsa.h; every step runs in li
     out, lse = forward(q, k, v, plan, mode)    # fsa_forward, mode "norm_bound" | "online_max"
     forward_ex(...)                            # fsa_forward_ex
     out, lse = forward_host(q, k, v, plan)     # fsa_forward_host (host tensors, overlapped copies)
+    q, k, v = prep(x, w, plan, H, ...)         # fsa_prep (RMS norm, QKV projection, rotary, packing, norms)
 
 The library is loaded lazily on first use; importing the package needs no GPU.
 """
 from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_SCRATCH_LIMIT, FSA_ERR_TIMEOUT,  # noqa: F401
                    FSA_ERR_UNSUPPORTED, FSA_OK,
-                   FsaError, Plan, forward, forward_ex, forward_host, load, new_stats, norms, norms_noalloc,
+                   FsaError, Plan, forward, forward_ex, forward_host, load, new_stats, norms, norms_noalloc, prep,
                    read_stats,
                    selftest_wait_timeout, status_string)
 
-__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "forward_host", "new_stats", "read_stats",
+__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "forward_host", "prep", "new_stats",
+           "read_stats",
            "selftest_wait_timeout",
            "status_string", "load", "FsaError"]

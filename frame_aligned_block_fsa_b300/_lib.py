@@ -28,7 +28,7 @@ FSA_ERR_SCRATCH_LIMIT = -5
 # Exported symbols, in the order include/fsa.h declares them.
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
            "fsa_plan_set_center_keys",
-           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_norms_noalloc",
+           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_prep", "fsa_norms_noalloc",
            "fsa_status_string", "fsa_selftest_wait_timeout")
 
 _lock = threading.Lock()
@@ -71,6 +71,8 @@ def load():
             lib.fsa_forward_ex.restype = i32
             lib.fsa_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, vp]
             lib.fsa_forward_host.restype = i32
+            lib.fsa_prep.argtypes = [vp, vp, i32, i32, i32, vp] + [vp] * 9
+            lib.fsa_prep.restype = i32
             lib.fsa_norms_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.fsa_norms_noalloc.restype = i32
             lib.fsa_status_string.argtypes = [i32]
@@ -239,6 +241,36 @@ def forward_host(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=No
     _check("fsa_forward_host", load().fsa_forward_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), H, D,
                                                        plan.handle, MODES[mode], int(heads_per_chunk), st))
     return out, lse
+
+
+def prep(x, w, plan: Plan, H: int, q=None, k=None, v=None, qnorm=None, kmax=None, bound=None, eligible=None,
+         stats=None, stream=None):
+    """fsa_prep: x bf16 [N, d_model], w bf16 [3 H 128, d_model] (device) -> (q, k, v) bf16
+    [H, N, 128], with the norms written to the given tensors (or kept in the plan)."""
+    import torch
+
+    if x.dim() != 2 or w.dim() != 2 or x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise ValueError("x and w must be 2-D bf16 tensors")
+    N, dm = x.shape
+    D = 128
+    if N != plan.N:
+        raise ValueError(f"sequence length {N} != plan F*T = {plan.N}")
+    if tuple(w.shape) != (3 * H * D, dm):
+        raise ValueError(f"w must be [{3 * H * D}, {dm}]")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous")
+    outs = []
+    for t in (q, k, v):
+        if t is None:
+            t = torch.empty((H, N, D), dtype=torch.bfloat16, device=x.device)
+        elif tuple(t.shape) != (H, N, D) or t.dtype != torch.bfloat16 or not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous bf16 [H, N, 128]")
+        outs.append(t)
+    st = _stream_handle(stream)
+    _check("fsa_prep", load().fsa_prep(_ptr(x), _ptr(w), dm, H, D, plan.handle, _ptr(outs[0]), _ptr(outs[1]),
+                                       _ptr(outs[2]), _ptr(qnorm), _ptr(kmax), _ptr(bound), _ptr(eligible),
+                                       _ptr(stats), st))
+    return tuple(outs)
 
 
 def new_stats(device):

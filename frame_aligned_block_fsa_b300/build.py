@@ -23,7 +23,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libfsa.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["fsa_attn.cu", "fsa_norms.cu", "fsa_norms_noalloc.cu"]
+CUDA_SOURCES = ["fsa_attn.cu", "fsa_norms.cu", "fsa_norms_noalloc.cu", "fsa_prep.cu"]
 HOST_SOURCES = ["fsa_api.cpp"]
 HEADERS = ["fsa_ptx.cuh", "fsa_internal.h"]
 

@@ -43,6 +43,14 @@ struct fsa_plan_s {
     bool tickets_fresh = false;  // newly allocated: zero them on the next norms launch
     float* d_mu = nullptr;       // [H][D] head key means (centred keys)
     unsigned* d_htickets = nullptr;
+    // fsa_prep workspace
+    int64_t cap_rinv = 0, cap_kpart = 0, cap_ks = 0, cap_kbar = 0;
+    float* d_rinv = nullptr;
+    float* d_kpart = nullptr;
+    float* d_ks = nullptr;
+    float* d_kbar = nullptr;
+    float2* d_rope = nullptr;    // [N][64] (cos, sin), built once per plan
+    int sms = 0;
     float* d_qnorm = nullptr;
     float* d_bound = nullptr;
     float* d_kmax = nullptr;
@@ -260,6 +268,44 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
     return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
 }
 
+constexpr float kPrepEps = 1e-6f;           // RMS-norm epsilon
+constexpr double kPrepRopeBase = 10000.0;   // rotary base
+
+// Workspace of fsa_prep: 1/rms per token, K column partials, per-query-frame key statistics,
+// and the rotary table (cos, sin of n * base^(-2i/128) for every token n and pair i < 64),
+// computed on the host in double precision once per plan.
+int ensure_prep_workspace(fsa_plan_s* P, int H)
+{
+    const int64_t nb32 = (P->N + 31) / 32;
+    const int64_t hf = static_cast<int64_t>(H) * P->F;
+    int rc;
+    if ((rc = grow(&P->d_rinv, &P->cap_rinv, P->N)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_kpart, &P->cap_kpart, static_cast<int64_t>(H) * nb32 * 2 * 128)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_ks, &P->cap_ks, hf)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_kbar, &P->cap_kbar, hf * 128)) != FSA_OK) return rc;
+    if (P->sms == 0 && cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    if (P->d_rope == nullptr) {
+        std::vector<float2> tab(static_cast<size_t>(P->N) * 64);
+        double theta[64];
+        for (int i = 0; i < 64; ++i) theta[i] = std::pow(kPrepRopeBase, -2.0 * i / 128.0);
+        for (int64_t n = 0; n < P->N; ++n)
+            for (int i = 0; i < 64; ++i) {
+                const double a = static_cast<double>(n) * theta[i];
+                tab[static_cast<size_t>(n) * 64 + i] = make_float2(static_cast<float>(std::cos(a)),
+                                                                   static_cast<float>(std::sin(a)));
+            }
+        float2* d = nullptr;
+        if (cudaMalloc(reinterpret_cast<void**>(&d), tab.size() * sizeof(float2)) != cudaSuccess) return FSA_ERR_CUDA;
+        if (cudaMemcpy(d, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+            cudaFree(d);
+            return FSA_ERR_CUDA;
+        }
+        P->d_rope = d;
+    }
+    return FSA_OK;
+}
+
 // Device copies of a host problem, streams and events for fsa_forward_host.
 int ensure_host_pipeline(fsa_plan_s* P, int H, int D, int chunks)
 {
@@ -447,6 +493,11 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_tickets);
         cudaFree(plan->d_htickets);
         cudaFree(plan->d_mu);
+        cudaFree(plan->d_rinv);
+        cudaFree(plan->d_kpart);
+        cudaFree(plan->d_ks);
+        cudaFree(plan->d_kbar);
+        cudaFree(plan->d_rope);
         cudaFree(plan->d_elig);
         cudaFree(plan->d_hq);
         cudaFree(plan->d_hk);
@@ -505,6 +556,68 @@ int fsa_norms(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t pla
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
     if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
     return run_norms(plan, q, k, H, D, qnorm, kmax, bound, eligible, static_cast<cudaStream_t>(stream));
+}
+
+int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fsa_plan_t plan, uint16_t* q,
+             uint16_t* k, uint16_t* v, float* qnorm, float* kmax, float* bound, uint8_t* eligible,
+             fsa_stats_t* dev_stats, void* stream)
+{
+    int rc = check_shape(plan, H, D);
+    if (rc != FSA_OK) return rc;
+    if (D != 128 || H % 2 != 0 || plan->center_keys) return FSA_ERR_UNSUPPORTED;
+    if (d_model <= 0 || d_model % 64 != 0) return FSA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(3) * H * D * d_model >= (int64_t(1) << 40)) return FSA_ERR_INVALID_ARG;
+    if (H == 0) return FSA_OK;
+    if (!x || !w || !q || !k || !v) return FSA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(q) || !aligned16(k) || !aligned16(v)) return FSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if ((rc = ensure_device(plan)) != FSA_OK) return rc;
+    if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
+    if ((rc = ensure_prep_workspace(plan, H)) != FSA_OK) return rc;
+    if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
+    float* km = kmax ? kmax : plan->d_kmax;
+    if ((rc = cuda_status(cudaMemsetAsync(km, 0, static_cast<size_t>(H) * plan->F * sizeof(float), st))) != FSA_OK)
+        return rc;
+    CUtensorMap mx, mw;
+    if ((rc = make_tensor_map(&mx, x, plan->N, d_model, 256)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mw, w, static_cast<int64_t>(3) * H * D, d_model, 256)) != FSA_OK) return rc;
+    fsa::PrepLaunch L;
+    L.tmX = &mx;
+    L.tmW = &mw;
+    L.x = x;
+    L.runs = plan->d_runs;
+    L.eps = kPrepEps;
+    L.sms = plan->sms;
+    L.stream = st;
+    fsa::PrepParams& p = L.params;
+    p.N = static_cast<int>(plan->N);
+    p.dm = d_model;
+    p.H = H;
+    p.T = plan->T;
+    p.F = plan->F;
+    p.m_tiles = static_cast<int>((plan->N + 255) / 256);
+    p.n_tile0 = 0;
+    p.n_tiles = 0;
+    p.rinv = plan->d_rinv;
+    p.rope = plan->d_rope;
+    p.q = q;
+    p.k = k;
+    p.v = v;
+    p.qnorm = qnorm;
+    p.bound = bound ? bound : plan->d_bound;
+    p.kmax = reinterpret_cast<unsigned*>(km);
+    p.kpart = plan->d_kpart;
+    p.ks = plan->d_ks;
+    p.kbar = plan->d_kbar;
+    p.gmax = plan->d_gmax;
+    p.scale = 1.0f / std::sqrt(static_cast<float>(D));
+    p.stats = dev_stats;
+    p.wait_limit = kDefaultWaitLimit;
+    if (fsa::launch_prep(L) != 0) return FSA_ERR_CUDA;
+    return fsa::launch_eligibility(plan->d_gmax, plan->tau, eligible ? eligible : plan->d_elig, H, st) == 0
+               ? FSA_OK
+               : FSA_ERR_CUDA;
 }
 
 int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,

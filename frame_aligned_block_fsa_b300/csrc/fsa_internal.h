@@ -75,6 +75,44 @@ int launch_norms(const NormsLaunch& L);
 constexpr int kMaxKeyChunks = 8;
 int norms_key_chunks(int T);
 
+int launch_eligibility(const unsigned* gmax, float tau, uint8_t* eligible, int H, cudaStream_t stream);
+
+// The fused preparation of the attention inputs (fsa_prep): D = 128, H even.
+struct PrepParams {
+    int N, dm, H, T, F;
+    int m_tiles;             // ceil(N / 256) token-row tiles
+    int n_tile0, n_tiles;    // output-column tiles of 256 handled by one launch
+    float* rinv;             // [N] 1 / rms of each token row
+    const float2* rope;      // [N][64] (cos, sin) of the rotary angles
+    uint16_t* q;             // [H][N][128] outputs
+    uint16_t* k;
+    uint16_t* v;
+    float* qnorm;            // [H][N] or null
+    float* bound;            // [H][N]
+    unsigned* kmax;          // [H][F] float bits; zero before the K/V launch
+    float* kpart;            // [H][ceil(N/32)][2][128] column sums of K per 32-row block and frame
+    float* ks;               // [H][F] max key norm over each query frame's key set
+    float* kbar;             // [H][F][128] mean key over each query frame's key set
+    unsigned* gmax;          // [H] gap maxima (float bits)
+    float scale;             // c = 1/sqrt(D)
+    fsa_stats_t* stats;      // or null
+    long long wait_limit;    // clock cycles
+};
+
+struct PrepLaunch {
+    const CUtensorMap* tmX;  // x bf16 [N][dm], boxes 64 x 256
+    const CUtensorMap* tmW;  // w bf16 [3 H 128][dm], boxes 64 x 256
+    const uint16_t* x;
+    const int32_t* runs;     // device [F][kRunStride]
+    float eps;
+    int sms;                 // persistent grid size
+    PrepParams params;
+    cudaStream_t stream;
+};
+
+int launch_prep(const PrepLaunch& L);
+int prep_smem_bytes();
+
 // Read-only view of a plan's host data, for entry points that live outside fsa_api.cpp.
 struct PlanView {
     int F, T;

@@ -413,6 +413,12 @@ static int launch_norms_d(const NormsLaunch& L)
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
+int launch_eligibility(const unsigned* gmax, float tau, uint8_t* eligible, int H, cudaStream_t stream)
+{
+    eligibility_kernel<<<(H + 127) / 128, 128, 0, stream>>>(gmax, tau, eligible, H);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
 int launch_norms(const NormsLaunch& L)
 {
     if (L.D == 64) return launch_norms_d<64>(L);

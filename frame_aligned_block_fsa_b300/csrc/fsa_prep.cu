@@ -1,0 +1,489 @@
+// fsa_prep.cu -- the attention's inputs prepared in one pass: RMS norm, QKV projection,
+// rotary embedding, head packing, and the bound's norms as a by-product.
+//
+// "HeyGen toi uu hoa mo hinh Avatar IV tren Google Cloud Trillium TPU" (aihot.vn), section
+// "Bo cuc la ABI", Fig. 5: the chain of small operations that produces the attention's inputs
+// (normalisation, rotary embeddings, projection, head packing) is fused into one kernel that
+// writes its output in exactly the layout the next step reads, so no repacking copies are
+// left between them.  Here the next step is the attention kernel: the projection's epilogue
+// writes Q, K and V as bf16 [H][N][D] (the layout of its TMA tensor maps) and, while the
+// values are in registers, the norms the norm-bound softmax needs (section "Giai phong
+// Softmax"), so no separate pass re-reads Q and K for them.
+//
+// Readings (the pages name the steps, not their exact form): RMS norm without a learned gain
+// (a gain folds into the weights); y = xhat W^T with W bf16 [3 H D][d_model] (q rows, then k,
+// then v, head-major); rotary embedding of q and k at position = token index, pairs
+// (i, i + D/2) turned by n * base^(-2i/D); v not rotated.
+//
+// Kernels, in stream order:
+//   rms_kernel          1 / rms of every token row (one warp per row)
+//   fsa_prep_kernel     the projection GEMM for the K and V columns: per tile, rotary,
+//                       bf16 rounding, the head-packed store, per-frame max key norms (an
+//                       atomic max) and per-32-row column sums of K (fixed-order partials)
+//   prep_reduce_kernel  per (query frame, head): max key norm and mean key over the frame's
+//                       key set, from the K launch's partials in a fixed order
+//   fsa_prep_kernel     the projection GEMM for the Q columns: rotary, rounding, store, and
+//                       per row ||q||, the bound c ||q|| Kmax_S and the gap statistic
+//                       c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head
+//   eligibility         (the norms' kernel) per head: gap maximum <= tau
+//
+// fsa_prep_kernel (persistent, one CTA per SM, 10 warps): a 256 x 256 output tile is two
+// M = 128 accumulators (token rows 0-127 and 128-255) of 256 fp32 TMEM columns each, built by
+// tcgen05.mma (kind::f16, bf16 inputs from 128-byte swizzled shared memory, K-major A and B)
+// over 64-wide K steps fed by TMA through a 3-stage ring.  The 256 columns are two heads of
+// q, k or v (H is even); each of the 8 epilogue warps owns 32 rows (its TMEM lane quarter of
+// one accumulator) and takes the two heads in turn: it reads the pairs (i, i + 64) of its rows
+// from TMEM, scales by 1/rms, rotates, rounds, and stores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "fsa_internal.h"
+#include "fsa_ptx.cuh"
+
+namespace fsa {
+
+namespace {
+
+constexpr int kPrepThreads = 320;  // 8 epilogue warps, the TMA warp, the MMA warp
+constexpr int kPrepWarpTma = 8, kPrepWarpMma = 9;
+
+struct PrepCfg {
+    static constexpr int BM = 256, BN = 256, BK = 64;
+    static constexpr int A_BYTES = BM * 128;  // 256 rows x 64 bf16 (one 128-byte swizzle panel)
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int NS = 3;
+    static constexpr int BAR_OFF = NS * STAGE_BYTES;
+    static constexpr int B_FULL = 0;              // NS: A and B of a stage landed
+    static constexpr int B_EMPTY = NS;            // NS: the MMAs reading a stage are done
+    static constexpr int B_ACC_FULL = 2 * NS;     // the tile's accumulators are complete
+    static constexpr int B_ACC_EMPTY = 2 * NS + 1;  // the epilogue has read them (8 arrivals)
+    static constexpr int B_DRAIN = 2 * NS + 2;
+    static constexpr int N_BARS = 2 * NS + 3;
+    static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;  // abort flag +0, TMEM address +8
+    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
+    static_assert(MISC_OFF + 16 <= BAR_OFF + 256, "reserved area");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(128, 256, false, false);
+};
+
+enum : int { SITE_PREP_EMPTY = 11, SITE_PREP_FULL = 12, SITE_PREP_ACC_EMPTY = 13, SITE_PREP_ACC_FULL = 14,
+             SITE_PREP_DRAIN = 15 };
+
+// After the call, lane l holds the sum over the warp's lanes of v[l] (five butterfly rounds,
+// each halving the values a lane keeps; the order of the additions is fixed).
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const bool up = lane & 16;
+        const float send = up ? v[i] : v[i + 16];
+        const float keep = up ? v[i + 16] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const bool up = lane & 8;
+        const float send = up ? v[i] : v[i + 8];
+        const float keep = up ? v[i + 8] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const bool up = lane & 4;
+        const float send = up ? v[i] : v[i + 4];
+        const float keep = up ? v[i + 4] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const bool up = lane & 2;
+        const float send = up ? v[i] : v[i + 2];
+        const float keep = up ? v[i + 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+    }
+    {
+        const bool up = lane & 1;
+        const float send = up ? v[0] : v[1];
+        const float keep = up ? v[1] : v[0];
+        v[0] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+    }
+    return v[0];
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// One epilogue warp: 32 token rows (n_first + lane) of one head of q (sect 0), k (1) or v (2),
+// read from TMEM at `trow` (this warp's lane quarter, the head's first column).
+__device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow, int sect, int h, int n_first,
+                                              int lane)
+{
+    const int n = n_first + lane;
+    const bool valid = n < p.N;
+    const int nn = valid ? n : p.N - 1;
+    const int f = nn / p.T;
+    const float ri = p.rinv[nn];
+    const float4* rope = reinterpret_cast<const float4*>(p.rope + static_cast<int64_t>(nn) * 64);
+    uint16_t* base = sect == 0 ? p.q : (sect == 1 ? p.k : p.v);
+    uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<int64_t>(h) * p.N + nn) * 128);
+    const float4* kbar = reinterpret_cast<const float4*>(p.kbar + (static_cast<int64_t>(h) * p.F + f) * 128);
+    // frame segments of the warp's rows (a 32-row block meets at most two frames, T >= 16)
+    const int f_lo = n_first / p.T;
+    const int n_last = min(n_first + 31, p.N - 1);
+    const bool straddle = n_last / p.T != f_lo;
+    const int64_t nb32 = (static_cast<int64_t>(p.N) + 31) / 32;
+    float* kpart = p.kpart + ((static_cast<int64_t>(h) * nb32 + n_first / 32) * 2) * 128;
+
+    float ss = 0.0f, dot = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        float a[16], b[16];
+        tmem_ld_x16(trow + 16 * c, a);
+        tmem_ld_x16(trow + 64 + 16 * c, b);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            reg_fence(a[i]);
+            reg_fence(b[i]);
+        }
+        if (sect < 2) {
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const float4 cs = __ldg(rope + 8 * c + i / 2);  // (cos, sin) of pairs 16c+i, 16c+i+1
+                const float x0 = a[i] * ri, y0 = b[i] * ri, x1 = a[i + 1] * ri, y1 = b[i + 1] * ri;
+                a[i] = x0 * cs.x - y0 * cs.y;
+                b[i] = x0 * cs.y + y0 * cs.x;
+                a[i + 1] = x1 * cs.z - y1 * cs.w;
+                b[i + 1] = x1 * cs.w + y1 * cs.z;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                a[i] *= ri;
+                b[i] *= ri;
+            }
+        }
+        uint32_t pa[8], pb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            pa[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+            pb[i] = pack_bf16x2(b[2 * i], b[2 * i + 1]);
+        }
+        if (valid) {
+            dst[2 * c] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+            dst[2 * c + 1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+            dst[8 + 2 * c] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+            dst[8 + 2 * c + 1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+        }
+        if (sect == 2) continue;
+        // the norms use the rounded values, the ones the attention kernel will read
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            ss = fmaf(bf16_lo(pa[i]), bf16_lo(pa[i]), ss);
+            ss = fmaf(bf16_hi(pa[i]), bf16_hi(pa[i]), ss);
+            ss = fmaf(bf16_lo(pb[i]), bf16_lo(pb[i]), ss);
+            ss = fmaf(bf16_hi(pb[i]), bf16_hi(pb[i]), ss);
+        }
+        if (sect == 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 ka = __ldg(kbar + 4 * c + i);       // columns 16c + 4i ..
+                const float4 kb = __ldg(kbar + 16 + 4 * c + i);  // columns 64 + 16c + 4i ..
+                dot = fmaf(bf16_lo(pa[2 * i]), ka.x, dot);
+                dot = fmaf(bf16_hi(pa[2 * i]), ka.y, dot);
+                dot = fmaf(bf16_lo(pa[2 * i + 1]), ka.z, dot);
+                dot = fmaf(bf16_hi(pa[2 * i + 1]), ka.w, dot);
+                dot = fmaf(bf16_lo(pb[2 * i]), kb.x, dot);
+                dot = fmaf(bf16_hi(pb[2 * i]), kb.y, dot);
+                dot = fmaf(bf16_lo(pb[2 * i + 1]), kb.z, dot);
+                dot = fmaf(bf16_hi(pb[2 * i + 1]), kb.w, dot);
+            }
+        } else {
+            // column sums of the warp's rows of each frame; lane l ends with column
+            // 16c + l (l < 16) or 64 + 16c + l - 16
+            const int col = lane < 16 ? 16 * c + lane : 64 + 16 * c + (lane - 16);
+            const bool in_lo = valid && f == f_lo;
+#pragma unroll 1
+            for (int side = straddle ? 1 : 0; side >= 0; --side) {
+                const bool take = side == 0 ? in_lo : (valid && !in_lo);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    v[2 * i] = take ? bf16_lo(pa[i]) : 0.0f;
+                    v[2 * i + 1] = take ? bf16_hi(pa[i]) : 0.0f;
+                    v[16 + 2 * i] = take ? bf16_lo(pb[i]) : 0.0f;
+                    v[16 + 2 * i + 1] = take ? bf16_hi(pb[i]) : 0.0f;
+                }
+                kpart[128 * side + col] = reduce_scatter32(v, lane);
+            }
+        }
+    }
+    if (sect == 2) return;
+    const float nrm = sqrtf(ss);
+    if (sect == 0) {
+        const float qk = nrm * p.ks[static_cast<int64_t>(h) * p.F + f];
+        const float gap = valid ? p.scale * (qk - dot) : 0.0f;
+        if (valid) {
+            p.bound[static_cast<int64_t>(h) * p.N + n] = p.scale * qk;
+            if (p.qnorm) p.qnorm[static_cast<int64_t>(h) * p.N + n] = nrm;
+        }
+        const float g = warp_max(gap);
+        if (lane == 0) atomicMax(p.gmax + h, __float_as_uint(fmaxf(g, 0.0f)));
+    } else {
+        const float m0 = warp_max(valid && f == f_lo ? nrm : 0.0f);
+        const float m1 = warp_max(valid && f != f_lo ? nrm : 0.0f);
+        if (lane == 0) {
+            // non-negative floats order like their bit patterns
+            atomicMax(p.kmax + static_cast<int64_t>(h) * p.F + f_lo, __float_as_uint(m0));
+            if (straddle) atomicMax(p.kmax + static_cast<int64_t>(h) * p.F + f_lo + 1, __float_as_uint(m1));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPrepThreads, 1)
+    fsa_prep_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                    const PrepParams p)
+{
+    using C = PrepCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_u32 = smem_u32(smem_raw);
+    const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
+    uint8_t* sgen = smem_raw + (sbase - raw_u32);
+    auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::MISC_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n_total = p.m_tiles * p.n_tiles;
+    const int KB = p.dm / C::BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(bar(C::B_FULL + s), 1);
+            mbar_init(bar(C::B_EMPTY + s), 1);
+        }
+        mbar_init(bar(C::B_ACC_FULL), 1);
+        mbar_init(bar(C::B_ACC_EMPTY), 8);  // one arrival per epilogue warp
+        mbar_init(bar(C::B_DRAIN), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kPrepWarpMma) {
+        tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tmem_slot;
+
+    WaitCtl wc;
+    wc.abort = abort_flag;
+    wc.err_word = p.stats ? &p.stats->error : nullptr;
+    wc.err_site = p.stats ? &p.stats->timeout_site : nullptr;
+    wc.limit = p.wait_limit;
+
+    if (warp == kPrepWarpTma) {
+        // ------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&tmX);
+            tma_prefetch_desc(&tmW);
+            uint32_t g = 0;  // K steps issued by this CTA
+            bool ok = true;
+            for (int t = blockIdx.x; t < n_total && ok; t += gridDim.x) {
+                const int m = t / p.n_tiles, nt = p.n_tile0 + t % p.n_tiles;
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int s = static_cast<int>(g % C::NS);
+                    if (!mbar_wait(bar(C::B_EMPTY + s), ((g / C::NS) & 1) ^ 1, wc, SITE_PREP_EMPTY)) {
+                        ok = false;
+                        break;
+                    }
+                    // rows of x past N are zero-filled (a ragged last row tile)
+                    mbar_arrive_expect_tx(bar(C::B_FULL + s), C::STAGE_BYTES);
+                    tma_load_2d(sbase + s * C::STAGE_BYTES, &tmX, kb * C::BK, m * C::BM, bar(C::B_FULL + s));
+                    tma_load_2d(sbase + s * C::STAGE_BYTES + C::A_BYTES, &tmW, kb * C::BK, nt * C::BN,
+                                bar(C::B_FULL + s));
+                    ++g;
+                }
+            }
+            // Every copy this thread issued must land before the CTA may exit.
+            for (uint32_t u = (g > C::NS ? g - C::NS : 0); u < g; ++u)
+                mbar_wait(bar(C::B_FULL + u % C::NS), (u / C::NS) & 1, wc, SITE_PREP_DRAIN, false);
+        }
+    } else if (warp == kPrepWarpMma) {
+        // ------------------------------------------------------------- MMA issuer
+        const bool leader = elect_one();
+        const uint64_t d0 = smem_desc_sw128(sbase, 16, 1024);
+        uint32_t g = 0;
+        int it = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < n_total && ok; t += gridDim.x, ++it) {
+            if (!mbar_wait(bar(C::B_ACC_EMPTY), (it & 1) ^ 1, wc, SITE_PREP_ACC_EMPTY)) break;
+            tc_fence_after();
+            for (int kb = 0; kb < KB; ++kb) {
+                const int s = static_cast<int>(g % C::NS);
+                if (!mbar_wait(bar(C::B_FULL + s), (g / C::NS) & 1, wc, SITE_PREP_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (leader) {
+#pragma unroll
+                    for (int j = 0; j < 2; ++j)
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            // 16 bf16 = 32 B along the 128-byte swizzle row; rows 128 j.. of A
+                            const uint64_t a = d0 + ((s * C::STAGE_BYTES + j * (C::A_BYTES / 2) + ks * 32) >> 4);
+                            const uint64_t b = d0 + ((s * C::STAGE_BYTES + C::A_BYTES + ks * 32) >> 4);
+                            mma_ss(tbase + 256u * j, a, b, C::IDESC, (kb > 0 || ks > 0) ? 1u : 0u);
+                        }
+                    tc_commit(bar(C::B_EMPTY + s));
+                }
+                __syncwarp();
+                ++g;
+            }
+            if (!ok) break;
+            if (leader) tc_commit(bar(C::B_ACC_FULL));
+            __syncwarp();
+        }
+        // every MMA this thread issued completes before TMEM is released
+        if (leader) tc_commit(bar(C::B_DRAIN));
+        __syncwarp();
+        mbar_wait(bar(C::B_DRAIN), 0, wc, SITE_PREP_DRAIN, false);
+    } else {
+        // ------------------------------------------------------------- epilogue
+        // warp w reads TMEM lane quarter w % 4 of accumulator w / 4, both heads in turn
+        const int qd = warp & 3, j = warp >> 2;
+        const uint32_t trow = tbase + (static_cast<uint32_t>(32 * qd) << 16) + 256u * j;
+        int it = 0;
+        for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++it) {
+            if (!mbar_wait(bar(C::B_ACC_FULL), it & 1, wc, SITE_PREP_ACC_FULL)) break;
+            tc_fence_after();
+            const int m = t / p.n_tiles, nt = p.n_tile0 + t % p.n_tiles;
+            const int n_first = m * C::BM + 128 * j + 32 * qd;
+#pragma unroll 1
+            for (int hh = 0; hh < 2 && n_first < p.N; ++hh) {
+                const int col0 = nt * C::BN + 128 * hh;  // first output column of the head
+                const int sect = col0 / (p.H * 128);
+                const int h = col0 / 128 - sect * p.H;
+                prep_epilogue(p, trow + 128u * hh, sect, h, n_first, lane);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_ACC_EMPTY));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kPrepWarpMma) {
+        tc_fence_after();
+        tmem_dealloc(tbase, C::TMEM_COLS);
+    }
+}
+
+// 1 / sqrt(mean(x^2) + eps) per token row, one warp per row, 16-byte loads.
+__global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x, int N, int dm, float eps,
+                                                  float* __restrict__ rinv)
+{
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= N) return;
+    const uint4* r = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(row) * dm);
+    float s = 0.0f;
+    for (int i = lane; i < dm / 8; i += 32) {
+        const uint4 u = __ldg(r + i);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float a = bf16_lo(w[k]), b = bf16_hi(w[k]);
+            s = fmaf(a, a, s);
+            s = fmaf(b, b, s);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) rinv[row] = 1.0f / sqrtf(s / static_cast<float>(dm) + eps);
+}
+
+// Per (query frame f, head h): Kmax_S = max over the key frames g in S(f) of kmax[h][g], and
+// kbar_S = (sum over g in S(f) of the frame's key sum) / (|S(f)| T), the frame sums added from
+// the 32-row partials in ascending row order.  Also zeroes the head's gap maximum (f == 0).
+__global__ void __launch_bounds__(128) prep_reduce_kernel(const float* __restrict__ kpart,
+                                                          const unsigned* __restrict__ kmax,
+                                                          const int32_t* __restrict__ runs, int N, int T, int F,
+                                                          float* __restrict__ ks, float* __restrict__ kbar,
+                                                          unsigned* __restrict__ gmax)
+{
+    const int f = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    const int64_t nb32 = (static_cast<int64_t>(N) + 31) / 32;
+    const float* part = kpart + static_cast<int64_t>(h) * nb32 * 2 * 128;
+    const int32_t* rr = runs + f * kRunStride;
+    float s = 0.0f, m = 0.0f;
+    int count = 0;
+    for (int r = 0; r < rr[0]; ++r) {
+        const int g0 = rr[1 + 2 * r] / T, ng = rr[2 + 2 * r] / T;
+        for (int g = g0; g < g0 + ng; ++g) {
+            const int64_t first = static_cast<int64_t>(g) * T, last = first + T - 1;
+            for (int64_t b = first / 32; b <= last / 32; ++b) {
+                // a block whose first row lies in an earlier frame holds frame g's rows in side 1
+                const int side = b * 32 < first ? 1 : 0;
+                s += part[(b * 2 + side) * 128 + d];
+            }
+            m = fmaxf(m, __uint_as_float(kmax[static_cast<int64_t>(h) * F + g]));
+        }
+        count += rr[2 + 2 * r];
+    }
+    kbar[(static_cast<int64_t>(h) * F + f) * 128 + d] = s / static_cast<float>(count);
+    if (d == 0) {
+        ks[static_cast<int64_t>(h) * F + f] = m;
+        if (f == 0) gmax[h] = 0u;
+    }
+}
+
+}  // namespace
+
+int prep_smem_bytes() { return PrepCfg::SMEM_BYTES; }
+
+int launch_prep(const PrepLaunch& L)
+{
+    static bool attr_done = false;
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(fsa_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PrepCfg::SMEM_BYTES) != cudaSuccess)
+            return -3;
+        attr_done = true;
+    }
+    const PrepParams& p0 = L.params;
+    rms_kernel<<<(p0.N + 7) / 8, 256, 0, L.stream>>>(L.x, p0.N, p0.dm, L.eps, const_cast<float*>(p0.rinv));
+    // K and V columns (tiles H/2 .. 3H/2 - 1 of 256 columns), then the key statistics
+    PrepParams pkv = p0;
+    pkv.n_tile0 = p0.H / 2;
+    pkv.n_tiles = p0.H;
+    const int tiles_kv = pkv.m_tiles * pkv.n_tiles;
+    fsa_prep_kernel<<<tiles_kv < L.sms ? tiles_kv : L.sms, kPrepThreads, PrepCfg::SMEM_BYTES, L.stream>>>(
+        *L.tmX, *L.tmW, pkv);
+    prep_reduce_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(p0.kpart, p0.kmax, L.runs, p0.N, p0.T, p0.F,
+                                                               const_cast<float*>(p0.ks),
+                                                               const_cast<float*>(p0.kbar), p0.gmax);
+    // Q columns (tiles 0 .. H/2 - 1), with the bound and the gap statistic
+    PrepParams pq = p0;
+    pq.n_tile0 = 0;
+    pq.n_tiles = p0.H / 2;
+    const int tiles_q = pq.m_tiles * pq.n_tiles;
+    fsa_prep_kernel<<<tiles_q < L.sms ? tiles_q : L.sms, kPrepThreads, PrepCfg::SMEM_BYTES, L.stream>>>(
+        *L.tmX, *L.tmW, pq);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace fsa

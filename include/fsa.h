@@ -203,6 +203,34 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
                      int H, int D, fsa_plan_t plan, int mode, int heads_per_chunk, void* stream);
 
 /*
+ * fsa_prep -- the attention's inputs from the hidden states, in one fused pass.
+ * Source: aihot.vn page above, "Bo cuc la ABI", Fig. 5: normalisation, rotary embeddings,
+ * projection and head packing fused into one kernel that writes exactly the layout the next
+ * step reads (no repacking copies in between).  Readings of this library:
+ *   xhat = x / sqrt(mean_c x_c^2 + 1e-6)            (RMS norm over d_model, no gain: fold a
+ *                                                   gain into w)
+ *   y    = xhat w^T                                 (w rows: q heads, then k, then v)
+ *   q, k of every head rotated at position n (the token index): pairs (i, i + D/2) turned
+ *        by n * 10000^(-2i/D); v not rotated
+ *   q, k, v written as bf16 [H][N][D], the layout fsa_forward* read.
+ * The projection's epilogue also produces the norms of fsa_norms for these q and k (from
+ * the bf16 values written), so no separate pass re-reads them:
+ *   qnorm[h][n], kmax[h][g], bound[h][n], eligible[h]   as in fsa_norms.
+ *   x: device bf16 [N][d_model] (N = F*T of the plan), d_model a multiple of 64;
+ *   w: device bf16 [3*H*D][d_model];  q, k, v: device bf16 [H][N][D] outputs;
+ *   qnorm (may be NULL), kmax, bound, eligible: device outputs, or NULL to keep them in the
+ *   plan's workspace;  dev_stats: optional, as in fsa_forward_ex (a bounded wait that gave
+ *   up records FSA_ERR_TIMEOUT there).
+ * All pointers 16-byte aligned.  Uses and may grow plan-owned workspace; the first call builds
+ * the plan's rotary table (N*64 (cos, sin) pairs) on the host and uploads it.
+ * Errors: FSA_ERR_INVALID_ARG (NULL or misaligned tensor, bad d_model), FSA_ERR_UNSUPPORTED
+ * (D != 128, odd H, mean-centred keys on the plan, device), FSA_ERR_CUDA.  H == 0 is a no-op.
+ */
+int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fsa_plan_t plan,
+             uint16_t* q, uint16_t* k, uint16_t* v, float* qnorm, float* kmax, float* bound,
+             uint8_t* eligible, fsa_stats_t* dev_stats, void* stream);
+
+/*
  * fsa_norms_noalloc -- fsa_norms for callers that cannot allocate device memory.
  * The pages have no counterpart; this is a service of the library.  fsa_norms keeps its
  * scratch (per-frame key sums, per-head maxima) in a plan workspace grown with cudaMalloc,
