@@ -272,8 +272,8 @@ constexpr float kPrepEps = 1e-6f;           // RMS-norm epsilon
 constexpr double kPrepRopeBase = 10000.0;   // rotary base
 
 // Workspace of fsa_prep: 1/rms per token, K column partials, per-query-frame key statistics,
-// and the rotary table (cos, sin of n * base^(-2i/128) for every token n and pair i < 64),
-// computed on the host in double precision once per plan.
+// and the rotary table (cos, sin of n * base^(-2i/128) for every token n, at least 32 rows, and
+// pair i < 64), computed on the host in double precision once per plan.
 int ensure_prep_workspace(fsa_plan_s* P, int H)
 {
     const int64_t nb32 = (P->N + 31) / 32;
@@ -286,10 +286,12 @@ int ensure_prep_workspace(fsa_plan_s* P, int H)
     if (P->sms == 0 && cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
         return FSA_ERR_CUDA;
     if (P->d_rope == nullptr) {
-        std::vector<float2> tab(static_cast<size_t>(P->N) * 64);
+        // at least 32 rows: the kernel builds every angle from row n_first and rows 0..31
+        const int64_t rows = std::max<int64_t>(P->N, 32);
+        std::vector<float2> tab(static_cast<size_t>(rows) * 64);
         double theta[64];
         for (int i = 0; i < 64; ++i) theta[i] = std::pow(kPrepRopeBase, -2.0 * i / 128.0);
-        for (int64_t n = 0; n < P->N; ++n)
+        for (int64_t n = 0; n < rows; ++n)
             for (int i = 0; i < 64; ++i) {
                 const double a = static_cast<double>(n) * theta[i];
                 tab[static_cast<size_t>(n) * 64 + i] = make_float2(static_cast<float>(std::cos(a)),

@@ -83,7 +83,7 @@ struct PrepParams {
     int m_tiles;             // ceil(N / 256) token-row tiles
     int n_tile0, n_tiles;    // output-column tiles of 256 handled by one launch
     float* rinv;             // [N] 1 / rms of each token row
-    const float2* rope;      // [N][64] (cos, sin) of the rotary angles
+    const float2* rope;      // [max(N, 32)][64] (cos, sin) of the rotary angles
     uint16_t* q;             // [H][N][128] outputs
     uint16_t* k;
     uint16_t* v;

@@ -63,8 +63,12 @@ struct PrepCfg {
     static constexpr int B_DRAIN = 2 * NS + 2;
     static constexpr int N_BARS = 2 * NS + 3;
     static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;  // abort flag +0, TMEM address +8
-    static constexpr int SMEM_BYTES = 1024 + BAR_OFF + 256;
     static_assert(MISC_OFF + 16 <= BAR_OFF + 256, "reserved area");
+    // rotary angles by addition: (cos, sin) of l * theta_i for l < 32 ([i][l], 16 KB) and of
+    // n_first * theta_i for each epilogue warp's first row ([warp][i], 4 KB)
+    static constexpr int DELTA_OFF = BAR_OFF + 256;
+    static constexpr int RBASE_OFF = DELTA_OFF + 64 * 32 * 8;
+    static constexpr int SMEM_BYTES = 1024 + RBASE_OFF + 8 * 64 * 8;
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(128, 256, false, false);
@@ -121,22 +125,32 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// 32-byte store (one full sector per lane); the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* ptr, const uint32_t* r)
+{
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(ptr), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // One epilogue warp: 32 token rows (n_first + lane) of one head of q (sect 0), k (1) or v (2),
-// read from TMEM at `trow` (this warp's lane quarter, the head's first column).
+// read from TMEM at `trow` (this warp's lane quarter, the head's first column).  The rotary
+// angle of row n_first + l and pair i is n_first theta_i + l theta_i: its cosine and sine come
+// from rbase[i] (the warp's first row) and delta[i][l] by the addition formulas.
 __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow, int sect, int h, int n_first,
-                                              int lane)
+                                              int lane, float ri, const float2* delta, const float2* rbase)
 {
     const int n = n_first + lane;
     const bool valid = n < p.N;
     const int nn = valid ? n : p.N - 1;
     const int f = nn / p.T;
-    const float ri = p.rinv[nn];
-    const float4* rope = reinterpret_cast<const float4*>(p.rope + static_cast<int64_t>(nn) * 64);
     uint16_t* base = sect == 0 ? p.q : (sect == 1 ? p.k : p.v);
     uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<int64_t>(h) * p.N + nn) * 128);
+    // rows are 256 bytes, so 32-byte stores need only a 32-byte aligned tensor (uniform test)
+    const bool wide = (reinterpret_cast<uintptr_t>(base) & 31u) == 0;
     const float4* kbar = reinterpret_cast<const float4*>(p.kbar + (static_cast<int64_t>(h) * p.F + f) * 128);
     // frame segments of the warp's rows (a 32-row block meets at most two frames, T >= 16)
     const int f_lo = n_first / p.T;
@@ -146,26 +160,36 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
     float* kpart = p.kpart + ((static_cast<int64_t>(h) * nb32 + n_first / 32) * 2) * 128;
 
     float ss = 0.0f, dot = 0.0f;
+    // chunk c: pairs 16c .. 16c+15, i.e. columns 16c.. and 64 + 16c..; the next chunk's TMEM
+    // loads are in flight while this one is processed
+    float na[16], nb[16];
+    tmem_ld_x16(trow, na);
+    tmem_ld_x16(trow + 64, nb);
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         float a[16], b[16];
-        tmem_ld_x16(trow + 16 * c, a);
-        tmem_ld_x16(trow + 64 + 16 * c, b);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            reg_fence(a[i]);
-            reg_fence(b[i]);
+            reg_fence(na[i]);
+            reg_fence(nb[i]);
+            a[i] = na[i];
+            b[i] = nb[i];
+        }
+        if (c < 3) {
+            tmem_ld_x16(trow + 16 * (c + 1), na);
+            tmem_ld_x16(trow + 64 + 16 * (c + 1), nb);
         }
         if (sect < 2) {
 #pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const float4 cs = __ldg(rope + 8 * c + i / 2);  // (cos, sin) of pairs 16c+i, 16c+i+1
-                const float x0 = a[i] * ri, y0 = b[i] * ri, x1 = a[i + 1] * ri, y1 = b[i + 1] * ri;
-                a[i] = x0 * cs.x - y0 * cs.y;
-                b[i] = x0 * cs.y + y0 * cs.x;
-                a[i + 1] = x1 * cs.z - y1 * cs.w;
-                b[i + 1] = x1 * cs.w + y1 * cs.z;
+            for (int i = 0; i < 16; ++i) {
+                const float2 cb = rbase[16 * c + i];               // same for every lane: broadcast
+                const float2 cd = delta[(16 * c + i) * 32 + lane];  // consecutive lanes: no conflict
+                const float cs = cb.x * cd.x - cb.y * cd.y;
+                const float sn = cb.y * cd.x + cb.x * cd.y;
+                const float x = a[i] * ri, y = b[i] * ri;
+                a[i] = x * cs - y * sn;
+                b[i] = x * sn + y * cs;
             }
         } else {
 #pragma unroll
@@ -181,10 +205,15 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
             pb[i] = pack_bf16x2(b[2 * i], b[2 * i + 1]);
         }
         if (valid) {
-            dst[2 * c] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
-            dst[2 * c + 1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-            dst[8 + 2 * c] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-            dst[8 + 2 * c + 1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+            if (wide) {
+                st_global_v8(dst + 2 * c, pa);
+                st_global_v8(dst + 8 + 2 * c, pb);
+            } else {
+                dst[2 * c] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
+                dst[2 * c + 1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
+                dst[8 + 2 * c] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                dst[8 + 2 * c + 1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+            }
         }
         if (sect == 2) continue;
         // the norms use the rounded values, the ones the attention kernel will read
@@ -366,18 +395,33 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         // warp w reads TMEM lane quarter w % 4 of accumulator w / 4, both heads in turn
         const int qd = warp & 3, j = warp >> 2;
         const uint32_t trow = tbase + (static_cast<uint32_t>(32 * qd) << 16) + 256u * j;
+        float2* delta = reinterpret_cast<float2*>(sgen + C::DELTA_OFF);
+        float2* rbase = reinterpret_cast<float2*>(sgen + C::RBASE_OFF) + 64 * warp;
+        // delta[i][l] = rotary table row l (the table has at least 32 rows)
+        for (int e = threadIdx.x; e < 64 * 32; e += 256) delta[(e & 63) * 32 + (e >> 6)] = p.rope[e];
+        asm volatile("bar.sync 1, 256;" ::: "memory");
         int it = 0;
         for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++it) {
-            if (!mbar_wait(bar(C::B_ACC_FULL), it & 1, wc, SITE_PREP_ACC_FULL)) break;
-            tc_fence_after();
             const int m = t / p.n_tiles, nt = p.n_tile0 + t % p.n_tiles;
             const int n_first = m * C::BM + 128 * j + 32 * qd;
+            // loads that do not depend on the accumulators are issued before waiting for them
+            const bool act = n_first < p.N;
+            const int nn = act ? min(n_first + lane, p.N - 1) : 0;
+            const float ri = p.rinv[nn];
+            const float2 r0 = p.rope[static_cast<int64_t>(act ? n_first : 0) * 64 + lane];
+            const float2 r1 = p.rope[static_cast<int64_t>(act ? n_first : 0) * 64 + 32 + lane];
+            if (!mbar_wait(bar(C::B_ACC_FULL), it & 1, wc, SITE_PREP_ACC_FULL)) break;
+            tc_fence_after();
+            __syncwarp();  // the previous tile's reads of rbase are done
+            rbase[lane] = r0;
+            rbase[32 + lane] = r1;
+            __syncwarp();
 #pragma unroll 1
-            for (int hh = 0; hh < 2 && n_first < p.N; ++hh) {
+            for (int hh = 0; hh < 2 && act; ++hh) {
                 const int col0 = nt * C::BN + 128 * hh;  // first output column of the head
                 const int sect = col0 / (p.H * 128);
                 const int h = col0 / 128 - sect * p.H;
-                prep_epilogue(p, trow + 128u * hh, sect, h, n_first, lane);
+                prep_epilogue(p, trow + 128u * hh, sect, h, n_first, lane, ri, delta, rbase);
             }
             tc_fence_before();
             __syncwarp();
