@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--mode", choices=["norm_bound", "online_max"], default="norm_bound")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--center-keys", action="store_true", help="mean-centred key norms in the bound")
+    ap.add_argument("--prep", action="store_true",
+                    help="step = fsa_prep (hidden states -> q, k, v and norms, d_model = H*D) + attention")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the online-max comparison and gap stats")
@@ -338,7 +340,7 @@ def main():
     import torch
 
     import frame_aligned_block_fsa_b300 as fsa
-    from frame_aligned_block_fsa_b300.inputs import make_qkv
+    from frame_aligned_block_fsa_b300.inputs import make_prep_inputs, make_qkv
     from frame_aligned_block_fsa_b300.workloads import WORKLOADS
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
@@ -365,11 +367,20 @@ def main():
     # active FLOPs: every active (query block, key block) pair does QK^T and PV, 2 * 2 B^2 D each
     flops_step = plan.nnz() * 4 * wl.block * wl.block * D * H
     stream = torch.cuda.current_stream()
+    if args.prep:
+        # hidden states and projection weights of d_model = H * D; q, k, v are overwritten by
+        # the prep every step
+        dm = H * D
+        x, w = (t.to(dev) for t in make_prep_inputs(N, dm, H, D, seed=rank_seed(wl, rank) + 1000))
+        prep_flops = 2 * N * dm * 3 * H * D
 
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        fsa.norms(q, k, plan, None, None, bound, elig, stream=stream)
+        if args.prep:
+            fsa.prep(x, w, plan, H, q=q, k=k, v=v, bound=bound, eligible=elig, stream=stream)
+        else:
+            fsa.norms(q, k, plan, None, None, bound, elig, stream=stream)
         if ev is not None:
             ev[1].record(stream)
         fsa.forward_ex(q, k, v, plan, args.mode, out=out, lse=lse, bound=bound, eligible=elig, stream=stream)
@@ -406,7 +417,7 @@ def main():
 
     # ---------------------------------------------------------------- end to end (host buffers)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.prep:
         # fsa_forward_host: pinned host q, k, v in, pinned host out, lse back; the library
         # pipelines chunks of heads over copy-in, compute and copy-out streams
         qp, kp, vp = q_h.pin_memory(), k_h.pin_memory(), v_h.pin_memory()
@@ -484,7 +495,8 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "mode": args.mode, "center_keys": args.center_keys,
-                   "step": "fsa_norms + attention, all heads",
+                   "step": ("fsa_prep (x [N, H*D] -> q, k, v, norms) + attention, all heads" if args.prep
+                            else "fsa_norms + attention, all heads"),
                    "l2": f"inputs {3 * H * N * D * 2 / 1e6:.0f} MB > 126 MB L2, no flush",
                    "active_flops_per_step": flops_step, "parallelism": f"independent batch per rank x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -497,11 +509,19 @@ def main():
                            "frac": norms_bytes / (norms_avg * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
                            "ms_avg": norms_avg, "algorithmic_bytes": norms_bytes},
         "clocks": clk,
-        # per step: 3 norm kernels (4 with centred keys) + the attention kernel
-        "gpu_launches": (5 if args.center_keys else 4) * args.steps,
+        # per step: 3 norm kernels (4 with centred keys), or the prep's 6 (rms, K/V projection,
+        # frame key sums, key-set statistics, Q projection, eligibility), + the attention kernel
+        "gpu_launches": (7 if args.prep else (5 if args.center_keys else 4)) * args.steps,
         "e2e": e2e,
     }
     line.update(extras)
+    if args.prep:
+        prep_avg = norms_avg
+        line.pop("norms_roofline")
+        line["prep_roofline"] = {"bound": "tensor", "achieved": prep_flops / (prep_avg * 1e-3) / 1e12,
+                                 "peak": peak, "unit": "TFLOP/s",
+                                 "frac": prep_flops / (prep_avg * 1e-3) / 1e12 / peak, "ms_avg": prep_avg,
+                                 "flops": prep_flops, "kernel": "fsa_prep_kernel (K/V launch + Q launch)"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_leg(wl, target_seconds=12.0)
     plan.close()

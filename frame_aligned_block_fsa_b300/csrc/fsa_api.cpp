@@ -589,6 +589,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     L.tmW = &mw;
     L.x = x;
     L.runs = plan->d_runs;
+    L.ksum = plan->d_ksum;
     L.eps = kPrepEps;
     L.sms = plan->sms;
     L.stream = st;

@@ -104,6 +104,7 @@ struct PrepLaunch {
     const CUtensorMap* tmW;  // w bf16 [3 H 128][dm], boxes 64 x 256
     const uint16_t* x;
     const int32_t* runs;     // device [F][kRunStride]
+    float* ksum;             // [H][F][128] workspace: per-frame key sums
     float eps;
     int sms;                 // persistent grid size
     PrepParams params;

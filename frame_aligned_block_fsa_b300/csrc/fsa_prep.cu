@@ -20,8 +20,9 @@
 //   fsa_prep_kernel     the projection GEMM for the K and V columns: per tile, rotary,
 //                       bf16 rounding, the head-packed store, per-frame max key norms (an
 //                       atomic max) and per-32-row column sums of K (fixed-order partials)
-//   prep_reduce_kernel  per (query frame, head): max key norm and mean key over the frame's
-//                       key set, from the K launch's partials in a fixed order
+//   prep_frame_sum      per (key frame, head): the frame's key sum from the K launch's partials
+//   prep_set_stats      per (query frame, head): max key norm and mean key over the frame's key
+//                       set (fixed orders throughout)
 //   fsa_prep_kernel     the projection GEMM for the Q columns: rotary, rounding, store, and
 //                       per row ||q||, the bound c ||q|| Kmax_S and the gap statistic
 //                       c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head
@@ -460,30 +461,50 @@ __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x
     if (lane == 0) rinv[row] = 1.0f / sqrtf(s / static_cast<float>(dm) + eps);
 }
 
-// Per (query frame f, head h): Kmax_S = max over the key frames g in S(f) of kmax[h][g], and
-// kbar_S = (sum over g in S(f) of the frame's key sum) / (|S(f)| T), the frame sums added from
-// the 32-row partials in ascending row order.  Also zeroes the head's gap maximum (f == 0).
-__global__ void __launch_bounds__(128) prep_reduce_kernel(const float* __restrict__ kpart,
-                                                          const unsigned* __restrict__ kmax,
-                                                          const int32_t* __restrict__ runs, int N, int T, int F,
-                                                          float* __restrict__ ks, float* __restrict__ kbar,
-                                                          unsigned* __restrict__ gmax)
+// Per (key frame g, head h): the frame's key sum, from the K launch's 32-row partials added in
+// ascending row order (16 loads in flight; the order of the sum does not depend on that).
+__global__ void __launch_bounds__(128) prep_frame_sum_kernel(const float* __restrict__ kpart, int N, int T, int F,
+                                                             float* __restrict__ ksum)
 {
-    const int f = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
+    const int g = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
     const int64_t nb32 = (static_cast<int64_t>(N) + 31) / 32;
     const float* part = kpart + static_cast<int64_t>(h) * nb32 * 2 * 128;
+    const int64_t first = static_cast<int64_t>(g) * T, last = first + T - 1;
+    const int64_t b0 = first / 32, b1 = last / 32;
+    float s = 0.0f;
+    for (int64_t bb = b0; bb <= b1; bb += 16) {
+        float x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int64_t b = bb + u;
+            // a block whose first row lies in an earlier frame holds frame g's rows in side 1
+            const int side = b * 32 < first ? 1 : 0;
+            x[u] = b <= b1 ? __ldg(part + (b * 2 + side) * 128 + d) : 0.0f;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u)
+            if (bb + u <= b1) s += x[u];
+    }
+    ksum[(static_cast<int64_t>(h) * F + g) * 128 + d] = s;
+}
+
+// Per (query frame f, head h): Kmax_S = max over the key frames g in S(f) of kmax[h][g], and
+// kbar_S = (sum over g in S(f), in run order, of the frame key sums) / (|S(f)| T).  Also zeroes
+// the head's gap maximum (f == 0) before the Q launch max-reduces into it.
+__global__ void __launch_bounds__(128) prep_set_stats_kernel(const float* __restrict__ ksum,
+                                                             const unsigned* __restrict__ kmax,
+                                                             const int32_t* __restrict__ runs, int T, int F,
+                                                             float* __restrict__ ks, float* __restrict__ kbar,
+                                                             unsigned* __restrict__ gmax)
+{
+    const int f = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
     const int32_t* rr = runs + f * kRunStride;
     float s = 0.0f, m = 0.0f;
     int count = 0;
     for (int r = 0; r < rr[0]; ++r) {
         const int g0 = rr[1 + 2 * r] / T, ng = rr[2 + 2 * r] / T;
         for (int g = g0; g < g0 + ng; ++g) {
-            const int64_t first = static_cast<int64_t>(g) * T, last = first + T - 1;
-            for (int64_t b = first / 32; b <= last / 32; ++b) {
-                // a block whose first row lies in an earlier frame holds frame g's rows in side 1
-                const int side = b * 32 < first ? 1 : 0;
-                s += part[(b * 2 + side) * 128 + d];
-            }
+            s += ksum[(static_cast<int64_t>(h) * F + g) * 128 + d];
             m = fmaxf(m, __uint_as_float(kmax[static_cast<int64_t>(h) * F + g]));
         }
         count += rr[2 + 2 * r];
@@ -517,9 +538,9 @@ int launch_prep(const PrepLaunch& L)
     const int tiles_kv = pkv.m_tiles * pkv.n_tiles;
     fsa_prep_kernel<<<tiles_kv < L.sms ? tiles_kv : L.sms, kPrepThreads, PrepCfg::SMEM_BYTES, L.stream>>>(
         *L.tmX, *L.tmW, pkv);
-    prep_reduce_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(p0.kpart, p0.kmax, L.runs, p0.N, p0.T, p0.F,
-                                                               const_cast<float*>(p0.ks),
-                                                               const_cast<float*>(p0.kbar), p0.gmax);
+    prep_frame_sum_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(p0.kpart, p0.N, p0.T, p0.F, L.ksum);
+    prep_set_stats_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(L.ksum, p0.kmax, L.runs, p0.T, p0.F, p0.ks,
+                                                                  p0.kbar, p0.gmax);
     // Q columns (tiles 0 .. H/2 - 1), with the bound and the gap statistic
     PrepParams pq = p0;
     pq.n_tile0 = 0;
