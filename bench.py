@@ -47,7 +47,8 @@ def parse():
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--center-keys", action="store_true", help="mean-centred key norms in the bound")
     ap.add_argument("--prep", action="store_true",
-                    help="step = fsa_prep (hidden states -> q, k, v and norms, d_model = H*D) + attention")
+                    help="step = fsa_prep (hidden states -> q, k, v and norms) + attention")
+    ap.add_argument("--d-model", type=int, default=0, help="prep model width (default H*D)")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle CPU-baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--no-extras", action="store_true", help="skip the online-max comparison and gap stats")
@@ -370,7 +371,7 @@ def main():
     if args.prep:
         # hidden states and projection weights of d_model = H * D; q, k, v are overwritten by
         # the prep every step
-        dm = H * D
+        dm = args.d_model or H * D
         x, w = (t.to(dev) for t in make_prep_inputs(N, dm, H, D, seed=rank_seed(wl, rank) + 1000))
         prep_flops = 2 * N * dm * 3 * H * D
 
@@ -495,7 +496,7 @@ def main():
         "warmup": max(args.warmup, 3), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": workload_desc(wl), "mode": args.mode, "center_keys": args.center_keys,
-                   "step": ("fsa_prep (x [N, H*D] -> q, k, v, norms) + attention, all heads" if args.prep
+                   "step": (f"fsa_prep (x [N, {dm}] -> q, k, v, norms) + attention, all heads" if args.prep
                             else "fsa_norms + attention, all heads"),
                    "l2": f"inputs {3 * H * N * D * 2 / 1e6:.0f} MB > 126 MB L2, no flush",
                    "active_flops_per_step": flops_step, "parallelism": f"independent batch per rank x{world}"},
