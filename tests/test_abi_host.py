@@ -144,3 +144,28 @@ def test_forward_rejects_bad_arguments_before_device_work(lib):
     with fsa.Plan(16, 3600, 1, 0, 144) as p:
         assert lib.fsa_forward(fake, fake, fake, fake, fake, 40000, 128, p.handle, 0, None) == \
             fsa.FSA_ERR_INVALID_ARG
+
+
+def test_prep_rejects_bad_arguments_before_device_work(lib):
+    # fake, never-dereferenced, 16-byte aligned addresses: every call fails in validation
+    fake = ctypes.c_void_p(1 << 20)
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    with fsa.Plan(4, 64, 1, 0, 16) as p:
+        h = p.handle
+
+        def call(x=fake, w=fake, dm=256, H=2, D=128, q=fake, k=fake, v=fake):
+            return lib.fsa_prep(x, w, dm, H, D, h, q, k, v, None, None, None, None, None, None)
+
+        assert call(D=64) == fsa.FSA_ERR_UNSUPPORTED          # only D = 128
+        assert call(H=3) == fsa.FSA_ERR_UNSUPPORTED           # two heads per 256-column tile
+        assert call(dm=100) == fsa.FSA_ERR_INVALID_ARG        # d_model a multiple of 64
+        assert call(dm=0) == fsa.FSA_ERR_INVALID_ARG
+        assert call(x=None) == fsa.FSA_ERR_INVALID_ARG
+        assert call(v=None) == fsa.FSA_ERR_INVALID_ARG
+        assert call(w=odd) == fsa.FSA_ERR_INVALID_ARG         # 16-byte alignment
+        assert call(q=odd) == fsa.FSA_ERR_INVALID_ARG
+        assert call(H=0) == fsa.FSA_OK                        # empty: nothing to do
+        p.set_center_keys(True)
+        assert call() == fsa.FSA_ERR_UNSUPPORTED              # centred keys: norms pass only
+    assert lib.fsa_prep(fake, fake, 256, 2, 128, None, fake, fake, fake, None, None, None, None, None,
+                        None) == fsa.FSA_ERR_INVALID_ARG
