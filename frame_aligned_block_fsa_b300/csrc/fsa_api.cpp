@@ -44,7 +44,8 @@ struct fsa_plan_s {
     float* d_mu = nullptr;       // [H][D] head key means (centred keys)
     unsigned* d_htickets = nullptr;
     // fsa_prep workspace
-    int64_t cap_rinv = 0, cap_kpart = 0, cap_ks = 0, cap_kbar = 0;
+    int64_t cap_rinv = 0, cap_kpart = 0, cap_ks = 0, cap_kbar = 0, cap_gsync = 0;
+    unsigned* d_gsync = nullptr;  // grid-barrier counters of the prep kernel
     float* d_rinv = nullptr;
     float* d_kpart = nullptr;
     float* d_ks = nullptr;
@@ -283,6 +284,7 @@ int ensure_prep_workspace(fsa_plan_s* P, int H)
     if ((rc = grow(&P->d_kpart, &P->cap_kpart, static_cast<int64_t>(H) * nb32 * 2 * 128)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_ks, &P->cap_ks, hf)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_kbar, &P->cap_kbar, hf * 128)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_gsync, &P->cap_gsync, int64_t(3))) != FSA_OK) return rc;
     if (P->sms == 0 && cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
         return FSA_ERR_CUDA;
     if (P->d_rope == nullptr) {
@@ -500,6 +502,7 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_ks);
         cudaFree(plan->d_kbar);
         cudaFree(plan->d_rope);
+        cudaFree(plan->d_gsync);
         cudaFree(plan->d_elig);
         cudaFree(plan->d_hq);
         cudaFree(plan->d_hk);
@@ -588,8 +591,6 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     L.tmX = &mx;
     L.tmW = &mw;
     L.x = x;
-    L.runs = plan->d_runs;
-    L.ksum = plan->d_ksum;
     L.eps = kPrepEps;
     L.sms = plan->sms;
     L.stream = st;
@@ -600,8 +601,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     p.T = plan->T;
     p.F = plan->F;
     p.m_tiles = static_cast<int>((plan->N + 255) / 256);
-    p.n_tile0 = 0;
-    p.n_tiles = 0;
+    p.tiles_kv = p.m_tiles * H;
     p.rinv = plan->d_rinv;
     p.rope = plan->d_rope;
     p.q = q;
@@ -614,6 +614,9 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     p.ks = plan->d_ks;
     p.kbar = plan->d_kbar;
     p.gmax = plan->d_gmax;
+    p.ksum = plan->d_ksum;
+    p.runs = plan->d_runs;
+    p.gsync = plan->d_gsync;
     p.scale = 1.0f / std::sqrt(static_cast<float>(D));
     p.stats = dev_stats;
     p.wait_limit = kDefaultWaitLimit;

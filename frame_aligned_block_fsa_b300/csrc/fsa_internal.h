@@ -81,7 +81,7 @@ int launch_eligibility(const unsigned* gmax, float tau, uint8_t* eligible, int H
 struct PrepParams {
     int N, dm, H, T, F;
     int m_tiles;             // ceil(N / 256) token-row tiles
-    int n_tile0, n_tiles;    // output-column tiles of 256 handled by one launch
+    int tiles_kv;            // m_tiles * H tiles of K and V columns, before m_tiles * H/2 of Q
     float* rinv;             // [N] 1 / rms of each token row
     const float2* rope;      // [max(N, 32)][64] (cos, sin) of the rotary angles
     uint16_t* q;             // [H][N][128] outputs
@@ -94,6 +94,9 @@ struct PrepParams {
     float* ks;               // [H][F] max key norm over each query frame's key set
     float* kbar;             // [H][F][128] mean key over each query frame's key set
     unsigned* gmax;          // [H] gap maxima (float bits)
+    float* ksum;             // [H][F][128] workspace: per-frame key sums
+    const int32_t* runs;     // device [F][kRunStride]
+    unsigned* gsync;         // [3] grid-barrier counters, zero before the launch
     float scale;             // c = 1/sqrt(D)
     fsa_stats_t* stats;      // or null
     long long wait_limit;    // clock cycles
@@ -103,10 +106,8 @@ struct PrepLaunch {
     const CUtensorMap* tmX;  // x bf16 [N][dm], boxes 64 x 256
     const CUtensorMap* tmW;  // w bf16 [3 H 128][dm], boxes 64 x 256
     const uint16_t* x;
-    const int32_t* runs;     // device [F][kRunStride]
-    float* ksum;             // [H][F][128] workspace: per-frame key sums
     float eps;
-    int sms;                 // persistent grid size
+    int sms;                 // persistent grid size (all CTAs co-resident: cooperative launch)
     PrepParams params;
     cudaStream_t stream;
 };

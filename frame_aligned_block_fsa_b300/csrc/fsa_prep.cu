@@ -17,15 +17,17 @@
 //
 // Kernels, in stream order:
 //   rms_kernel          1 / rms of every token row (one warp per row)
-//   fsa_prep_kernel     the projection GEMM for the K and V columns: per tile, rotary,
-//                       bf16 rounding, the head-packed store, per-frame max key norms (an
-//                       atomic max) and per-32-row column sums of K (fixed-order partials)
-//   prep_frame_sum      per (key frame, head): the frame's key sum from the K launch's partials
-//   prep_set_stats      per (query frame, head): max key norm and mean key over the frame's key
-//                       set (fixed orders throughout)
-//   fsa_prep_kernel     the projection GEMM for the Q columns: rotary, rounding, store, and
-//                       per row ||q||, the bound c ||q|| Kmax_S and the gap statistic
-//                       c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head
+//   fsa_prep_kernel     the projection GEMM, one cooperative launch, tiles of the K and V
+//                       columns first, then of the Q columns.  K/V tile epilogues: rotary, bf16
+//                       rounding, the head-packed store, per-frame max key norms (an atomic
+//                       max) and per-32-row column sums of K (fixed-order partials).  Before its
+//                       first Q epilogue every CTA meets the others at a grid barrier; then the
+//                       CTAs share out the per-frame key sums and, after a second barrier, the
+//                       max key norm and mean key of every query frame's key set (fixed orders
+//                       throughout), and meet a third time.  Q tile epilogues: rotary, rounding,
+//                       store, and per row ||q||, the bound c ||q|| Kmax_S and the gap statistic
+//                       c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head.  The mainloop of a
+//                       CTA's first Q tile runs while its epilogue warps are at the barriers.
 //   eligibility         (the norms' kernel) per head: gap maximum <= tau
 //
 // fsa_prep_kernel (persistent, one CTA per SM, 10 warps): a 256 x 256 output tile is two
@@ -76,7 +78,112 @@ struct PrepCfg {
 };
 
 enum : int { SITE_PREP_EMPTY = 11, SITE_PREP_FULL = 12, SITE_PREP_ACC_EMPTY = 13, SITE_PREP_ACC_FULL = 14,
-             SITE_PREP_DRAIN = 15 };
+             SITE_PREP_DRAIN = 15, SITE_PREP_GRID = 16 };
+
+// Output tile t: token-row tile m and 256-column tile nt (K and V tiles first, then Q).
+__device__ __forceinline__ void prep_tile(const PrepParams& p, int t, int& m, int& nt)
+{
+    if (t < p.tiles_kv) {
+        m = t / p.H;
+        nt = p.H / 2 + t % p.H;
+    } else {
+        const int u = t - p.tiles_kv;
+        m = u / (p.H / 2);
+        nt = u % (p.H / 2);
+    }
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// All CTAs' 256 epilogue threads meet here (every CTA of the launch is resident: cooperative
+// launch).  Bounded: a wait that gives up raises the CTA's abort flag and records the site.
+__device__ __forceinline__ void grid_sync(unsigned* counter, unsigned n, int et, const WaitCtl& wc)
+{
+    __threadfence();  // this thread's writes (and atomics) are visible device-wide
+    __syncwarp();     // the warp is converged for the aligned barrier
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (et == 0) {
+        __threadfence();
+        atomicAdd(counter, 1u);
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(counter) < n) {
+            if (*wc.abort) break;
+            if (clock64() - t0 > wc.limit) {
+                *wc.abort = 1;
+                if (wc.err_word) atomicCAS(wc.err_word, 0, -4 /* FSA_ERR_TIMEOUT */);
+                if (wc.err_site) atomicCAS(wc.err_site, 0, SITE_PREP_GRID);
+                break;
+            }
+        }
+    }
+    __syncwarp();
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    __threadfence();
+}
+
+// Between the K/V and the Q epilogues: the per-frame key sums from the 32-row partials (added
+// in ascending row order, 16 loads in flight), then per query frame f the max key norm and the
+// mean key over its key set S(f) (frames in run order), shared out over all CTAs' epilogue
+// threads.  Also zeroes the gap maxima before any Q epilogue max-reduces into them.
+__device__ void prep_key_stats(const PrepParams& p, int et, const WaitCtl& wc)
+{
+    const unsigned n = gridDim.x;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
+    const int64_t total = static_cast<int64_t>(p.H) * p.F * 128;
+    const int64_t nb32 = (static_cast<int64_t>(p.N) + 31) / 32;
+    grid_sync(p.gsync + 0, n, et, wc);  // every K tile's partials and maxima are written
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + et; e < total; e += stride) {
+        const int d = static_cast<int>(e % 128);
+        const int64_t hg = e / 128;
+        const int g = static_cast<int>(hg % p.F), h = static_cast<int>(hg / p.F);
+        const float* part = p.kpart + static_cast<int64_t>(h) * nb32 * 2 * 128;
+        const int64_t first = static_cast<int64_t>(g) * p.T, last = first + p.T - 1;
+        const int64_t b0 = first / 32, b1 = last / 32;
+        float s = 0.0f;
+        for (int64_t bb = b0; bb <= b1; bb += 16) {
+            float x[16];
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int64_t b = bb + u;
+                // a block whose first row lies in an earlier frame holds frame g's rows in side 1
+                const int side = b * 32 < first ? 1 : 0;
+                x[u] = b <= b1 ? __ldcg(part + (b * 2 + side) * 128 + d) : 0.0f;
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+                if (bb + u <= b1) s += x[u];
+        }
+        p.ksum[e] = s;
+    }
+    grid_sync(p.gsync + 1, n, et, wc);  // every frame sum is written
+    for (int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + et; e < total; e += stride) {
+        const int d = static_cast<int>(e % 128);
+        const int64_t hf = e / 128;
+        const int f = static_cast<int>(hf % p.F), h = static_cast<int>(hf / p.F);
+        const int32_t* rr = p.runs + f * kRunStride;
+        float s = 0.0f, m = 0.0f;
+        int count = 0;
+        for (int r = 0; r < rr[0]; ++r) {
+            const int g0 = rr[1 + 2 * r] / p.T, ng = rr[2 + 2 * r] / p.T;
+            for (int g = g0; g < g0 + ng; ++g) {
+                s += __ldcg(p.ksum + (static_cast<int64_t>(h) * p.F + g) * 128 + d);
+                m = fmaxf(m, __uint_as_float(__ldcg(p.kmax + static_cast<int64_t>(h) * p.F + g)));
+            }
+            count += rr[2 + 2 * r];
+        }
+        p.kbar[e] = s / static_cast<float>(count);
+        if (d == 0) {
+            p.ks[hf] = m;
+            if (f == 0) p.gmax[h] = 0u;
+        }
+    }
+    grid_sync(p.gsync + 2, n, et, wc);  // the key-set statistics are written
+}
 
 // After the call, lane l holds the sum over the warp's lanes of v[l] (five butterfly rounds,
 // each halving the values a lane keeps; the order of the additions is fixed).
@@ -228,8 +335,9 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
         if (sect == 0) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float4 ka = __ldg(kbar + 4 * c + i);       // columns 16c + 4i ..
-                const float4 kb = __ldg(kbar + 16 + 4 * c + i);  // columns 64 + 16c + 4i ..
+                // written earlier in this launch by other CTAs: read from L2, not through L1
+                const float4 ka = __ldcg(kbar + 4 * c + i);       // columns 16c + 4i ..
+                const float4 kb = __ldcg(kbar + 16 + 4 * c + i);  // columns 64 + 16c + 4i ..
                 dot = fmaf(bf16_lo(pa[2 * i]), ka.x, dot);
                 dot = fmaf(bf16_hi(pa[2 * i]), ka.y, dot);
                 dot = fmaf(bf16_lo(pa[2 * i + 1]), ka.z, dot);
@@ -262,7 +370,7 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
     if (sect == 2) return;
     const float nrm = sqrtf(ss);
     if (sect == 0) {
-        const float qk = nrm * p.ks[static_cast<int64_t>(h) * p.F + f];
+        const float qk = nrm * __ldcg(p.ks + static_cast<int64_t>(h) * p.F + f);
         const float gap = valid ? p.scale * (qk - dot) : 0.0f;
         if (valid) {
             p.bound[static_cast<int64_t>(h) * p.N + n] = p.scale * qk;
@@ -295,7 +403,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_total = p.m_tiles * p.n_tiles;
+    const int n_total = p.tiles_kv + p.m_tiles * (p.H / 2);
     const int KB = p.dm / C::BK;
 
     if (threadIdx.x == 0) {
@@ -332,7 +440,8 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             uint32_t g = 0;  // K steps issued by this CTA
             bool ok = true;
             for (int t = blockIdx.x; t < n_total && ok; t += gridDim.x) {
-                const int m = t / p.n_tiles, nt = p.n_tile0 + t % p.n_tiles;
+                int m, nt;
+                prep_tile(p, t, m, nt);
                 for (int kb = 0; kb < KB; ++kb) {
                     const int s = static_cast<int>(g % C::NS);
                     if (!mbar_wait(bar(C::B_EMPTY + s), ((g / C::NS) & 1) ^ 1, wc, SITE_PREP_EMPTY)) {
@@ -402,8 +511,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         for (int e = threadIdx.x; e < 64 * 32; e += 256) delta[(e & 63) * 32 + (e >> 6)] = p.rope[e];
         asm volatile("bar.sync 1, 256;" ::: "memory");
         int it = 0;
+        bool stats_done = false;
         for (int t = blockIdx.x; t < n_total; t += gridDim.x, ++it) {
-            const int m = t / p.n_tiles, nt = p.n_tile0 + t % p.n_tiles;
+            // Every epilogue warp calls prep_key_stats exactly once (here, or after the loop if it
+            // left the loop early), so the named barriers inside it always match.
+            if (t >= p.tiles_kv && !stats_done) {
+                prep_key_stats(p, threadIdx.x, wc);
+                stats_done = true;
+            }
+            int m, nt;
+            prep_tile(p, t, m, nt);
             const int n_first = m * C::BM + 128 * j + 32 * qd;
             // loads that do not depend on the accumulators are issued before waiting for them
             const bool act = n_first < p.N;
@@ -428,6 +545,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_ACC_EMPTY));
         }
+        // a CTA with no Q tile, or whose epilogue stopped early, still takes its share of the
+        // key statistics and arrives at the grid barriers (after an abort without waiting)
+        if (!stats_done) prep_key_stats(p, threadIdx.x, wc);
     }
     tc_fence_before();
     __syncthreads();
@@ -461,61 +581,6 @@ __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x
     if (lane == 0) rinv[row] = 1.0f / sqrtf(s / static_cast<float>(dm) + eps);
 }
 
-// Per (key frame g, head h): the frame's key sum, from the K launch's 32-row partials added in
-// ascending row order (16 loads in flight; the order of the sum does not depend on that).
-__global__ void __launch_bounds__(128) prep_frame_sum_kernel(const float* __restrict__ kpart, int N, int T, int F,
-                                                             float* __restrict__ ksum)
-{
-    const int g = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-    const int64_t nb32 = (static_cast<int64_t>(N) + 31) / 32;
-    const float* part = kpart + static_cast<int64_t>(h) * nb32 * 2 * 128;
-    const int64_t first = static_cast<int64_t>(g) * T, last = first + T - 1;
-    const int64_t b0 = first / 32, b1 = last / 32;
-    float s = 0.0f;
-    for (int64_t bb = b0; bb <= b1; bb += 16) {
-        float x[16];
-#pragma unroll
-        for (int u = 0; u < 16; ++u) {
-            const int64_t b = bb + u;
-            // a block whose first row lies in an earlier frame holds frame g's rows in side 1
-            const int side = b * 32 < first ? 1 : 0;
-            x[u] = b <= b1 ? __ldg(part + (b * 2 + side) * 128 + d) : 0.0f;
-        }
-#pragma unroll
-        for (int u = 0; u < 16; ++u)
-            if (bb + u <= b1) s += x[u];
-    }
-    ksum[(static_cast<int64_t>(h) * F + g) * 128 + d] = s;
-}
-
-// Per (query frame f, head h): Kmax_S = max over the key frames g in S(f) of kmax[h][g], and
-// kbar_S = (sum over g in S(f), in run order, of the frame key sums) / (|S(f)| T).  Also zeroes
-// the head's gap maximum (f == 0) before the Q launch max-reduces into it.
-__global__ void __launch_bounds__(128) prep_set_stats_kernel(const float* __restrict__ ksum,
-                                                             const unsigned* __restrict__ kmax,
-                                                             const int32_t* __restrict__ runs, int T, int F,
-                                                             float* __restrict__ ks, float* __restrict__ kbar,
-                                                             unsigned* __restrict__ gmax)
-{
-    const int f = blockIdx.x, h = blockIdx.y, d = threadIdx.x;
-    const int32_t* rr = runs + f * kRunStride;
-    float s = 0.0f, m = 0.0f;
-    int count = 0;
-    for (int r = 0; r < rr[0]; ++r) {
-        const int g0 = rr[1 + 2 * r] / T, ng = rr[2 + 2 * r] / T;
-        for (int g = g0; g < g0 + ng; ++g) {
-            s += ksum[(static_cast<int64_t>(h) * F + g) * 128 + d];
-            m = fmaxf(m, __uint_as_float(kmax[static_cast<int64_t>(h) * F + g]));
-        }
-        count += rr[2 + 2 * r];
-    }
-    kbar[(static_cast<int64_t>(h) * F + f) * 128 + d] = s / static_cast<float>(count);
-    if (d == 0) {
-        ks[static_cast<int64_t>(h) * F + f] = m;
-        if (f == 0) gmax[h] = 0u;
-    }
-}
-
 }  // namespace
 
 int prep_smem_bytes() { return PrepCfg::SMEM_BYTES; }
@@ -529,25 +594,18 @@ int launch_prep(const PrepLaunch& L)
             return -3;
         attr_done = true;
     }
-    const PrepParams& p0 = L.params;
-    rms_kernel<<<(p0.N + 7) / 8, 256, 0, L.stream>>>(L.x, p0.N, p0.dm, L.eps, const_cast<float*>(p0.rinv));
-    // K and V columns (tiles H/2 .. 3H/2 - 1 of 256 columns), then the key statistics
-    PrepParams pkv = p0;
-    pkv.n_tile0 = p0.H / 2;
-    pkv.n_tiles = p0.H;
-    const int tiles_kv = pkv.m_tiles * pkv.n_tiles;
-    fsa_prep_kernel<<<tiles_kv < L.sms ? tiles_kv : L.sms, kPrepThreads, PrepCfg::SMEM_BYTES, L.stream>>>(
-        *L.tmX, *L.tmW, pkv);
-    prep_frame_sum_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(p0.kpart, p0.N, p0.T, p0.F, L.ksum);
-    prep_set_stats_kernel<<<dim3(p0.F, p0.H), 128, 0, L.stream>>>(L.ksum, p0.kmax, L.runs, p0.T, p0.F, p0.ks,
-                                                                  p0.kbar, p0.gmax);
-    // Q columns (tiles 0 .. H/2 - 1), with the bound and the gap statistic
-    PrepParams pq = p0;
-    pq.n_tile0 = 0;
-    pq.n_tiles = p0.H / 2;
-    const int tiles_q = pq.m_tiles * pq.n_tiles;
-    fsa_prep_kernel<<<tiles_q < L.sms ? tiles_q : L.sms, kPrepThreads, PrepCfg::SMEM_BYTES, L.stream>>>(
-        *L.tmX, *L.tmW, pq);
+    const PrepParams& p = L.params;
+    rms_kernel<<<(p.N + 7) / 8, 256, 0, L.stream>>>(L.x, p.N, p.dm, L.eps, p.rinv);
+    if (cudaMemsetAsync(p.gsync, 0, 3 * sizeof(unsigned), L.stream) != cudaSuccess) return -3;
+    // One CTA per SM, all resident at once (the grid barriers need it; a cooperative launch
+    // refuses a grid that cannot be).
+    const int total = p.tiles_kv + p.m_tiles * (p.H / 2);
+    const int grid = total < L.sms ? total : L.sms;
+    PrepParams pp = p;
+    void* args[] = {const_cast<CUtensorMap*>(L.tmX), const_cast<CUtensorMap*>(L.tmW), &pp};
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fsa_prep_kernel), dim3(grid), dim3(kPrepThreads),
+                                    args, PrepCfg::SMEM_BYTES, L.stream) != cudaSuccess)
+        return -3;
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
