@@ -66,6 +66,23 @@ def test_plan_matches_oracle_edge_shapes(lib, oracle_mod, shape):
     assert np.array_equal(row_ptr, o_row) and np.array_equal(col_idx, o_col)
 
 
+def test_plan_matches_oracle_on_random_shapes(lib, oracle_mod):
+    # 60 seeded shapes: frame counts 1..12, T a multiple of 16 up to 160, any window, any
+    # reference frame, every block size that divides T
+    rng = np.random.default_rng(2024)
+    for _ in range(60):
+        F = int(rng.integers(1, 13))
+        T = 16 * int(rng.integers(1, 11))
+        w = int(rng.integers(0, F + 2))
+        ref = int(rng.integers(0, F))
+        blocks = [b for b in range(16, T + 1, 16) if T % b == 0]
+        B = int(blocks[rng.integers(0, len(blocks))])
+        with fsa.Plan(F, T, w, ref, B) as p:
+            row_ptr, col_idx = p.export()
+        o_row, o_col = oracle_mod.plan(F, T, w, ref, B)
+        assert np.array_equal(row_ptr, o_row) and np.array_equal(col_idx, o_col), (F, T, w, ref, B)
+
+
 @pytest.mark.parametrize("args", [
     (0, 64, 1, 0, 16),      # no frames
     (4, 0, 1, 0, 16),       # no tokens
