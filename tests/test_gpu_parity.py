@@ -243,6 +243,21 @@ def test_forward_host_equals_device_bitwise(dev, mode, heads_per_chunk, pinned):
             assert torch.equal(lse, ref["lse_t"].cpu())
 
 
+def test_forward_host_with_centred_keys_equals_device_bitwise(dev):
+    # the plan option reaches the host pipeline: each chunk's norms centre its own heads' keys
+    # on their own means, so the chunked result equals the one device call bit for bit
+    wl = WORKLOADS["small"]
+    q, k, v = make_qkv(wl.H, wl.N, wl.D, seed=44, kind="offset")
+    ref = _gpu(dev, q, k, v, wl.F, wl.T, wl.w, wl.ref, wl.block, "norm_bound", stats=True, center_keys=True)
+    assert ref["stats"]["fallback_heads"] == 0
+    with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+        plan.set_center_keys(True)
+        out, lse = fsa.forward_host(q.pin_memory(), k.pin_memory(), v.pin_memory(), plan, "norm_bound",
+                                    heads_per_chunk=3)
+        torch.cuda.current_stream().synchronize()
+    assert torch.equal(out, ref["out_t"].cpu()) and torch.equal(lse, ref["lse_t"].cpu())
+
+
 @pytest.mark.parametrize("mode", ["norm_bound", "online_max"])
 @pytest.mark.parametrize("shape", [(2, 3, 1200, 64, 1, 0, 80), (4, 4, 384, 128, 1, 3, 128)])
 def test_repeated_runs_are_bitwise_identical(dev, oracle_mod, shape, mode):

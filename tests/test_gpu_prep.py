@@ -140,3 +140,30 @@ def test_prep_is_deterministic_and_feeds_the_attention(dev):
     do = (o1 - o2).abs()
     assert float(do.max()) <= 1e-3 and float(do.mean()) <= 1e-5
     assert float((l1 - l2).abs().max()) <= 1e-4
+
+
+@pytest.mark.parametrize("mode", ["norm_bound", "online_max"])
+def test_prep_then_attention_matches_the_oracle_chain(dev, oracle_mod, mode):
+    # The whole widened path: hidden states -> fsa_prep (q, k, v, bound, eligibility) ->
+    # attention with those norms, against the oracle's prep (rounded to bf16, as stored) followed
+    # by the oracle's attention.  A q, k or v element may sit one bf16 step from the oracle's
+    # rounding; that moves out and lse far less than the attention tolerance.
+    F, T, w_win, ref, block, H, dm = 4, 96, 1, 2, 32, 2, 256
+    N = F * T
+    x, w = make_prep_inputs(N, dm, H, D, seed=68)
+    exp = oracle_mod.prep_full(x, w, H, D)
+    qr, kr, vr = (torch.tensor(exp[n]).to(torch.bfloat16) for n in ("q", "k", "v"))
+    att = oracle_mod.attention_full(qr, kr, vr, F, T, w_win, ref)
+    with fsa.Plan(F, T, w_win, ref, block) as plan:
+        bd = torch.empty((H, N), device=dev)
+        el = torch.empty(H, dtype=torch.uint8, device=dev)
+        q, k, v = fsa.prep(x.to(dev), w.to(dev), plan, H, bound=bd, eligible=el)
+        st = fsa.new_stats(dev)
+        out, lse = fsa.forward_ex(q, k, v, plan, mode, bound=bd, eligible=el, stats=st)
+        torch.cuda.synchronize()
+    stats = fsa.read_stats(st)
+    assert stats["error"] == 0 and stats["fallback_heads"] == 0
+    d = np.abs(out.cpu().double().numpy() - att["out"])
+    dl = np.abs(lse.cpu().double().numpy() - att["lse"])
+    assert d.max() <= 1e-2 and d.mean() <= 1e-3, (d.max(), d.mean())
+    assert dl.max() <= 1e-2 and dl.mean() <= 1e-3, (dl.max(), dl.mean())
