@@ -13,14 +13,17 @@
  * (aihot.vn), section "Xoa bo mat na" (window + reference frame, block size a
  * multiple of 16 that divides a frame, Fig. 3) and section "Giai phong Softmax"
  * (fixed per-row upper bound from precomputed norms instead of a running max,
- * per-head fallback to the running max inside the same kernel, Fig. 4).
+ * per-head fallback to the running max inside the same kernel, optional mean-centred
+ * keys, Fig. 4).  fsa_prep also prepares q, k, v from the hidden states in one fused
+ * pass (section "Bo cuc la ABI", Fig. 5).
  *
  * Layouts (all row-major, contiguous, caller-owned device memory):
  *   q, k, v   bf16 [H][N][D], passed as 16-bit patterns (uint16_t), 16-byte aligned
  *   out       fp32 [H][N][D]
  *   lse       fp32 [H][N]   (natural log)
  *   qnorm     fp32 [H][N],  kmax fp32 [H][F],  bound fp32 [H][N],  eligible uint8 [H]
- * D must be 64 or 128.  H*N must stay below 2^31.
+ *   x         bf16 [N][d_model] and w bf16 [3*H*D][d_model] (fsa_prep only)
+ * D must be 64 or 128 (128 for fsa_prep).  H*N must stay below 2^31.
  *
  * Streams: every device call is asynchronous on the given stream (a cudaStream_t
  * passed as void*; NULL = legacy default stream).  Nothing synchronises the host
@@ -54,7 +57,7 @@ enum fsa_status {
     FSA_ERR_SCRATCH_LIMIT = -5 /* fsa_norms_noalloc: the problem needs more than its fixed scratch */
 };
 
-/* Device-side statistics, written by fsa_forward_ex when the caller passes a
+/* Device-side statistics, written by fsa_forward_ex and fsa_prep when the caller passes a
  * device pointer to one of these.  The call zeroes it first (on the stream). */
 typedef struct fsa_stats {
     int32_t error;          /* 0, or FSA_ERR_TIMEOUT if a bounded wait inside a kernel gave up */
