@@ -245,14 +245,16 @@ def forward_host(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=No
 
 def prep(x, w, plan: Plan, H: int, q=None, k=None, v=None, qnorm=None, kmax=None, bound=None, eligible=None,
          stats=None, stream=None):
-    """fsa_prep: x bf16 [N, d_model], w bf16 [3 H 128, d_model] (device) -> (q, k, v) bf16
-    [H, N, 128], with the norms written to the given tensors (or kept in the plan)."""
+    """fsa_prep: x bf16 [N, d_model], w bf16 [3 H D, d_model] (device; D = w rows / 3H) ->
+    (q, k, v) bf16 [H, N, D], with the norms written to the given tensors (or kept in the plan)."""
     import torch
 
     if x.dim() != 2 or w.dim() != 2 or x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
         raise ValueError("x and w must be 2-D bf16 tensors")
     N, dm = x.shape
-    D = 128
+    if H <= 0 or w.shape[0] % (3 * H):
+        raise ValueError("w must have 3 H D rows")
+    D = w.shape[0] // (3 * H)
     if N != plan.N:
         raise ValueError(f"sequence length {N} != plan F*T = {plan.N}")
     if tuple(w.shape) != (3 * H * D, dm):
@@ -264,7 +266,7 @@ def prep(x, w, plan: Plan, H: int, q=None, k=None, v=None, qnorm=None, kmax=None
         if t is None:
             t = torch.empty((H, N, D), dtype=torch.bfloat16, device=x.device)
         elif tuple(t.shape) != (H, N, D) or t.dtype != torch.bfloat16 or not t.is_contiguous():
-            raise ValueError("q, k, v must be contiguous bf16 [H, N, 128]")
+            raise ValueError(f"q, k, v must be contiguous bf16 [H, N, {D}]")
         outs.append(t)
     st = _stream_handle(stream)
     _check("fsa_prep", load().fsa_prep(_ptr(x), _ptr(w), dm, H, D, plan.handle, _ptr(outs[0]), _ptr(outs[1]),

@@ -45,6 +45,7 @@ struct fsa_plan_s {
     unsigned* d_htickets = nullptr;
     // fsa_prep workspace
     int64_t cap_rinv = 0, cap_kpart = 0, cap_ks = 0, cap_kbar = 0, cap_gsync = 0;
+    int rope_d = 0;               // head dim the rotary table was built for
     unsigned* d_gsync = nullptr;  // grid-barrier counters of the prep kernel
     float* d_rinv = nullptr;
     float* d_kpart = nullptr;
@@ -275,29 +276,33 @@ constexpr double kPrepRopeBase = 10000.0;   // rotary base
 // Workspace of fsa_prep: 1/rms per token, K column partials, per-query-frame key statistics,
 // and the rotary table (cos, sin of n * base^(-2i/128) for every token n, at least 32 rows, and
 // pair i < 64), computed on the host in double precision once per plan.
-int ensure_prep_workspace(fsa_plan_s* P, int H)
+int ensure_prep_workspace(fsa_plan_s* P, int H, int D)
 {
     const int64_t nb32 = (P->N + 31) / 32;
     const int64_t hf = static_cast<int64_t>(H) * P->F;
     int rc;
     if ((rc = grow(&P->d_rinv, &P->cap_rinv, P->N)) != FSA_OK) return rc;
-    if ((rc = grow(&P->d_kpart, &P->cap_kpart, static_cast<int64_t>(H) * nb32 * 2 * 128)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_kpart, &P->cap_kpart, static_cast<int64_t>(H) * nb32 * 2 * D)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_ks, &P->cap_ks, hf)) != FSA_OK) return rc;
-    if ((rc = grow(&P->d_kbar, &P->cap_kbar, hf * 128)) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_kbar, &P->cap_kbar, hf * D)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_gsync, &P->cap_gsync, int64_t(3))) != FSA_OK) return rc;
     if (P->sms == 0 && cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
         return FSA_ERR_CUDA;
-    if (P->d_rope == nullptr) {
+    if (P->d_rope == nullptr || P->rope_d != D) {
+        cudaFree(P->d_rope);
+        P->d_rope = nullptr;
+        P->rope_d = 0;
         // at least 32 rows: the kernel builds every angle from row n_first and rows 0..31
         const int64_t rows = std::max<int64_t>(P->N, 32);
-        std::vector<float2> tab(static_cast<size_t>(rows) * 64);
-        double theta[64];
-        for (int i = 0; i < 64; ++i) theta[i] = std::pow(kPrepRopeBase, -2.0 * i / 128.0);
+        const int half = D / 2;
+        std::vector<float2> tab(static_cast<size_t>(rows) * half);
+        std::vector<double> theta(half);
+        for (int i = 0; i < half; ++i) theta[i] = std::pow(kPrepRopeBase, -2.0 * i / D);
         for (int64_t n = 0; n < rows; ++n)
-            for (int i = 0; i < 64; ++i) {
+            for (int i = 0; i < half; ++i) {
                 const double a = static_cast<double>(n) * theta[i];
-                tab[static_cast<size_t>(n) * 64 + i] = make_float2(static_cast<float>(std::cos(a)),
-                                                                   static_cast<float>(std::sin(a)));
+                tab[static_cast<size_t>(n) * half + i] = make_float2(static_cast<float>(std::cos(a)),
+                                                                     static_cast<float>(std::sin(a)));
             }
         float2* d = nullptr;
         if (cudaMalloc(reinterpret_cast<void**>(&d), tab.size() * sizeof(float2)) != cudaSuccess) return FSA_ERR_CUDA;
@@ -306,6 +311,7 @@ int ensure_prep_workspace(fsa_plan_s* P, int H)
             return FSA_ERR_CUDA;
         }
         P->d_rope = d;
+        P->rope_d = D;
     }
     return FSA_OK;
 }
@@ -569,7 +575,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
 {
     int rc = check_shape(plan, H, D);
     if (rc != FSA_OK) return rc;
-    if (D != 128 || H % 2 != 0 || plan->center_keys) return FSA_ERR_UNSUPPORTED;
+    if ((D != 64 && D != 128) || (H * D) % 256 != 0 || plan->center_keys) return FSA_ERR_UNSUPPORTED;
     if (d_model <= 0 || d_model % 64 != 0) return FSA_ERR_INVALID_ARG;
     if (static_cast<int64_t>(3) * H * D * d_model >= (int64_t(1) << 40)) return FSA_ERR_INVALID_ARG;
     if (H == 0) return FSA_OK;
@@ -579,7 +585,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     std::lock_guard<std::mutex> lock(plan->mu);
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
     if ((rc = ensure_workspace(plan, H, D)) != FSA_OK) return rc;
-    if ((rc = ensure_prep_workspace(plan, H)) != FSA_OK) return rc;
+    if ((rc = ensure_prep_workspace(plan, H, D)) != FSA_OK) return rc;
     if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
     float* km = kmax ? kmax : plan->d_kmax;
     if ((rc = cuda_status(cudaMemsetAsync(km, 0, static_cast<size_t>(H) * plan->F * sizeof(float), st))) != FSA_OK)
@@ -592,6 +598,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     L.tmW = &mw;
     L.x = x;
     L.eps = kPrepEps;
+    L.D = D;
     L.sms = plan->sms;
     L.stream = st;
     fsa::PrepParams& p = L.params;
@@ -601,7 +608,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
     p.T = plan->T;
     p.F = plan->F;
     p.m_tiles = static_cast<int>((plan->N + 255) / 256);
-    p.tiles_kv = p.m_tiles * H;
+    p.tiles_kv = p.m_tiles * (H * D / 128);
     p.rinv = plan->d_rinv;
     p.rope = plan->d_rope;
     p.q = q;

@@ -77,24 +77,24 @@ int norms_key_chunks(int T);
 
 int launch_eligibility(const unsigned* gmax, float tau, uint8_t* eligible, int H, cudaStream_t stream);
 
-// The fused preparation of the attention inputs (fsa_prep): D = 128, H even.
+// The fused preparation of the attention inputs (fsa_prep): D = 64 or 128, H D a multiple of 256.
 struct PrepParams {
     int N, dm, H, T, F;
     int m_tiles;             // ceil(N / 256) token-row tiles
-    int tiles_kv;            // m_tiles * H tiles of K and V columns, before m_tiles * H/2 of Q
+    int tiles_kv;            // m_tiles * H D / 128 tiles of K and V columns, before the Q tiles
     float* rinv;             // [N] 1 / rms of each token row
-    const float2* rope;      // [max(N, 32)][64] (cos, sin) of the rotary angles
-    uint16_t* q;             // [H][N][128] outputs
+    const float2* rope;      // [max(N, 32)][D/2] (cos, sin) of the rotary angles
+    uint16_t* q;             // [H][N][D] outputs
     uint16_t* k;
     uint16_t* v;
     float* qnorm;            // [H][N] or null
     float* bound;            // [H][N]
     unsigned* kmax;          // [H][F] float bits; zero before the K/V launch
-    float* kpart;            // [H][ceil(N/32)][2][128] column sums of K per 32-row block and frame
+    float* kpart;            // [H][ceil(N/32)][2][D] column sums of K per 32-row block and frame
     float* ks;               // [H][F] max key norm over each query frame's key set
-    float* kbar;             // [H][F][128] mean key over each query frame's key set
+    float* kbar;             // [H][F][D] mean key over each query frame's key set
     unsigned* gmax;          // [H] gap maxima (float bits)
-    float* ksum;             // [H][F][128] workspace: per-frame key sums
+    float* ksum;             // [H][F][D] workspace: per-frame key sums
     const int32_t* runs;     // device [F][kRunStride]
     unsigned* gsync;         // [3] grid-barrier counters, zero before the launch
     float scale;             // c = 1/sqrt(D)
@@ -104,8 +104,9 @@ struct PrepParams {
 
 struct PrepLaunch {
     const CUtensorMap* tmX;  // x bf16 [N][dm], boxes 64 x 256
-    const CUtensorMap* tmW;  // w bf16 [3 H 128][dm], boxes 64 x 256
+    const CUtensorMap* tmW;  // w bf16 [3 H D][dm], boxes 64 x 256
     const uint16_t* x;
+    int D;                   // head dim, 64 or 128
     float eps;
     int sms;                 // persistent grid size (all CTAs co-resident: cooperative launch)
     PrepParams params;

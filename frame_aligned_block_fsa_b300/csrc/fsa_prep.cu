@@ -80,16 +80,19 @@ struct PrepCfg {
 enum : int { SITE_PREP_EMPTY = 11, SITE_PREP_FULL = 12, SITE_PREP_ACC_EMPTY = 13, SITE_PREP_ACC_FULL = 14,
              SITE_PREP_DRAIN = 15, SITE_PREP_GRID = 16 };
 
-// Output tile t: token-row tile m and 256-column tile nt (K and V tiles first, then Q).
+// Output tile t: token-row tile m and 256-column tile nt (K and V tiles first, then Q).  Each
+// of the q, k and v sections spans H D / 256 column tiles.
+template <int D>
 __device__ __forceinline__ void prep_tile(const PrepParams& p, int t, int& m, int& nt)
 {
+    const int ts = p.H * D / 256;
     if (t < p.tiles_kv) {
-        m = t / p.H;
-        nt = p.H / 2 + t % p.H;
+        m = t / (2 * ts);
+        nt = ts + t % (2 * ts);
     } else {
         const int u = t - p.tiles_kv;
-        m = u / (p.H / 2);
-        nt = u % (p.H / 2);
+        m = u / ts;
+        nt = u % ts;
     }
 }
 
@@ -130,18 +133,19 @@ __device__ __forceinline__ void grid_sync(unsigned* counter, unsigned n, int et,
 // in ascending row order, 16 loads in flight), then per query frame f the max key norm and the
 // mean key over its key set S(f) (frames in run order), shared out over all CTAs' epilogue
 // threads.  Also zeroes the gap maxima before any Q epilogue max-reduces into them.
+template <int D>
 __device__ void prep_key_stats(const PrepParams& p, int et, const WaitCtl& wc)
 {
     const unsigned n = gridDim.x;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * 256;
-    const int64_t total = static_cast<int64_t>(p.H) * p.F * 128;
+    const int64_t total = static_cast<int64_t>(p.H) * p.F * D;
     const int64_t nb32 = (static_cast<int64_t>(p.N) + 31) / 32;
     grid_sync(p.gsync + 0, n, et, wc);  // every K tile's partials and maxima are written
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + et; e < total; e += stride) {
-        const int d = static_cast<int>(e % 128);
-        const int64_t hg = e / 128;
+        const int d = static_cast<int>(e % D);
+        const int64_t hg = e / D;
         const int g = static_cast<int>(hg % p.F), h = static_cast<int>(hg / p.F);
-        const float* part = p.kpart + static_cast<int64_t>(h) * nb32 * 2 * 128;
+        const float* part = p.kpart + static_cast<int64_t>(h) * nb32 * 2 * D;
         const int64_t first = static_cast<int64_t>(g) * p.T, last = first + p.T - 1;
         const int64_t b0 = first / 32, b1 = last / 32;
         float s = 0.0f;
@@ -152,7 +156,7 @@ __device__ void prep_key_stats(const PrepParams& p, int et, const WaitCtl& wc)
                 const int64_t b = bb + u;
                 // a block whose first row lies in an earlier frame holds frame g's rows in side 1
                 const int side = b * 32 < first ? 1 : 0;
-                x[u] = b <= b1 ? __ldcg(part + (b * 2 + side) * 128 + d) : 0.0f;
+                x[u] = b <= b1 ? __ldcg(part + (b * 2 + side) * D + d) : 0.0f;
             }
 #pragma unroll
             for (int u = 0; u < 16; ++u)
@@ -162,8 +166,8 @@ __device__ void prep_key_stats(const PrepParams& p, int et, const WaitCtl& wc)
     }
     grid_sync(p.gsync + 1, n, et, wc);  // every frame sum is written
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * 256 + et; e < total; e += stride) {
-        const int d = static_cast<int>(e % 128);
-        const int64_t hf = e / 128;
+        const int d = static_cast<int>(e % D);
+        const int64_t hf = e / D;
         const int f = static_cast<int>(hf % p.F), h = static_cast<int>(hf / p.F);
         const int32_t* rr = p.runs + f * kRunStride;
         float s = 0.0f, m = 0.0f;
@@ -171,7 +175,7 @@ __device__ void prep_key_stats(const PrepParams& p, int et, const WaitCtl& wc)
         for (int r = 0; r < rr[0]; ++r) {
             const int g0 = rr[1 + 2 * r] / p.T, ng = rr[2 + 2 * r] / p.T;
             for (int g = g0; g < g0 + ng; ++g) {
-                s += __ldcg(p.ksum + (static_cast<int64_t>(h) * p.F + g) * 128 + d);
+                s += __ldcg(p.ksum + (static_cast<int64_t>(h) * p.F + g) * D + d);
                 m = fmaxf(m, __uint_as_float(__ldcg(p.kmax + static_cast<int64_t>(h) * p.F + g)));
             }
             count += rr[2 + 2 * r];
@@ -248,33 +252,36 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // read from TMEM at `trow` (this warp's lane quarter, the head's first column).  The rotary
 // angle of row n_first + l and pair i is n_first theta_i + l theta_i: its cosine and sine come
 // from rbase[i] (the warp's first row) and delta[i][l] by the addition formulas.
+template <int D>
 __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow, int sect, int h, int n_first,
                                               int lane, float ri, const float2* delta, const float2* rbase)
 {
+    constexpr int HALF = D / 2;     // rotary pairs (i, i + D/2)
+    constexpr int CHUNKS = D / 32;  // 16 pairs a chunk
     const int n = n_first + lane;
     const bool valid = n < p.N;
     const int nn = valid ? n : p.N - 1;
     const int f = nn / p.T;
     uint16_t* base = sect == 0 ? p.q : (sect == 1 ? p.k : p.v);
-    uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<int64_t>(h) * p.N + nn) * 128);
-    // rows are 256 bytes, so 32-byte stores need only a 32-byte aligned tensor (uniform test)
+    uint4* dst = reinterpret_cast<uint4*>(base + (static_cast<int64_t>(h) * p.N + nn) * D);
+    // rows are 2 D bytes, so 32-byte stores need only a 32-byte aligned tensor (uniform test)
     const bool wide = (reinterpret_cast<uintptr_t>(base) & 31u) == 0;
-    const float4* kbar = reinterpret_cast<const float4*>(p.kbar + (static_cast<int64_t>(h) * p.F + f) * 128);
+    const float4* kbar = reinterpret_cast<const float4*>(p.kbar + (static_cast<int64_t>(h) * p.F + f) * D);
     // frame segments of the warp's rows (a 32-row block meets at most two frames, T >= 16)
     const int f_lo = n_first / p.T;
     const int n_last = min(n_first + 31, p.N - 1);
     const bool straddle = n_last / p.T != f_lo;
     const int64_t nb32 = (static_cast<int64_t>(p.N) + 31) / 32;
-    float* kpart = p.kpart + ((static_cast<int64_t>(h) * nb32 + n_first / 32) * 2) * 128;
+    float* kpart = p.kpart + ((static_cast<int64_t>(h) * nb32 + n_first / 32) * 2) * D;
 
     float ss = 0.0f, dot = 0.0f;
-    // chunk c: pairs 16c .. 16c+15, i.e. columns 16c.. and 64 + 16c..; the next chunk's TMEM
+    // chunk c: pairs 16c .. 16c+15, i.e. columns 16c.. and D/2 + 16c..; the next chunk's TMEM
     // loads are in flight while this one is processed
     float na[16], nb[16];
     tmem_ld_x16(trow, na);
-    tmem_ld_x16(trow + 64, nb);
+    tmem_ld_x16(trow + HALF, nb);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < CHUNKS; ++c) {
         float a[16], b[16];
         tmem_ld_wait();
 #pragma unroll
@@ -284,9 +291,9 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
             a[i] = na[i];
             b[i] = nb[i];
         }
-        if (c < 3) {
+        if (c + 1 < CHUNKS) {
             tmem_ld_x16(trow + 16 * (c + 1), na);
-            tmem_ld_x16(trow + 64 + 16 * (c + 1), nb);
+            tmem_ld_x16(trow + HALF + 16 * (c + 1), nb);
         }
         if (sect < 2) {
 #pragma unroll
@@ -315,12 +322,12 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
         if (valid) {
             if (wide) {
                 st_global_v8(dst + 2 * c, pa);
-                st_global_v8(dst + 8 + 2 * c, pb);
+                st_global_v8(dst + HALF / 8 + 2 * c, pb);
             } else {
                 dst[2 * c] = make_uint4(pa[0], pa[1], pa[2], pa[3]);
                 dst[2 * c + 1] = make_uint4(pa[4], pa[5], pa[6], pa[7]);
-                dst[8 + 2 * c] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
-                dst[8 + 2 * c + 1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
+                dst[HALF / 8 + 2 * c] = make_uint4(pb[0], pb[1], pb[2], pb[3]);
+                dst[HALF / 8 + 2 * c + 1] = make_uint4(pb[4], pb[5], pb[6], pb[7]);
             }
         }
         if (sect == 2) continue;
@@ -336,8 +343,8 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 // written earlier in this launch by other CTAs: read from L2, not through L1
-                const float4 ka = __ldcg(kbar + 4 * c + i);       // columns 16c + 4i ..
-                const float4 kb = __ldcg(kbar + 16 + 4 * c + i);  // columns 64 + 16c + 4i ..
+                const float4 ka = __ldcg(kbar + 4 * c + i);             // columns 16c + 4i ..
+                const float4 kb = __ldcg(kbar + HALF / 4 + 4 * c + i);  // columns D/2 + 16c + 4i ..
                 dot = fmaf(bf16_lo(pa[2 * i]), ka.x, dot);
                 dot = fmaf(bf16_hi(pa[2 * i]), ka.y, dot);
                 dot = fmaf(bf16_lo(pa[2 * i + 1]), ka.z, dot);
@@ -349,8 +356,8 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
             }
         } else {
             // column sums of the warp's rows of each frame; lane l ends with column
-            // 16c + l (l < 16) or 64 + 16c + l - 16
-            const int col = lane < 16 ? 16 * c + lane : 64 + 16 * c + (lane - 16);
+            // 16c + l (l < 16) or D/2 + 16c + l - 16
+            const int col = lane < 16 ? 16 * c + lane : HALF + 16 * c + (lane - 16);
             const bool in_lo = valid && f == f_lo;
 #pragma unroll 1
             for (int side = straddle ? 1 : 0; side >= 0; --side) {
@@ -363,7 +370,7 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
                     v[16 + 2 * i] = take ? bf16_lo(pb[i]) : 0.0f;
                     v[16 + 2 * i + 1] = take ? bf16_hi(pb[i]) : 0.0f;
                 }
-                kpart[128 * side + col] = reduce_scatter32(v, lane);
+                kpart[D * side + col] = reduce_scatter32(v, lane);
             }
         }
     }
@@ -389,6 +396,7 @@ __device__ __forceinline__ void prep_epilogue(const PrepParams& p, uint32_t trow
     }
 }
 
+template <int D>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     fsa_prep_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                     const PrepParams p)
@@ -403,7 +411,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n_total = p.tiles_kv + p.m_tiles * (p.H / 2);
+    const int n_total = p.tiles_kv + p.m_tiles * (p.H * D / 256);
     const int KB = p.dm / C::BK;
 
     if (threadIdx.x == 0) {
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             bool ok = true;
             for (int t = blockIdx.x; t < n_total && ok; t += gridDim.x) {
                 int m, nt;
-                prep_tile(p, t, m, nt);
+                prep_tile<D>(p, t, m, nt);
                 for (int kb = 0; kb < KB; ++kb) {
                     const int s = static_cast<int>(g % C::NS);
                     if (!mbar_wait(bar(C::B_EMPTY + s), ((g / C::NS) & 1) ^ 1, wc, SITE_PREP_EMPTY)) {
@@ -502,13 +510,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         mbar_wait(bar(C::B_DRAIN), 0, wc, SITE_PREP_DRAIN, false);
     } else {
         // ------------------------------------------------------------- epilogue
-        // warp w reads TMEM lane quarter w % 4 of accumulator w / 4, both heads in turn
+        // warp w reads TMEM lane quarter w % 4 of accumulator w / 4, its 256 / D heads in turn
+        constexpr int HALF = D / 2;
         const int qd = warp & 3, j = warp >> 2;
         const uint32_t trow = tbase + (static_cast<uint32_t>(32 * qd) << 16) + 256u * j;
         float2* delta = reinterpret_cast<float2*>(sgen + C::DELTA_OFF);
         float2* rbase = reinterpret_cast<float2*>(sgen + C::RBASE_OFF) + 64 * warp;
-        // delta[i][l] = rotary table row l (the table has at least 32 rows)
-        for (int e = threadIdx.x; e < 64 * 32; e += 256) delta[(e & 63) * 32 + (e >> 6)] = p.rope[e];
+        // delta[i][l] = rotary table row l, pair i (the table has at least 32 rows of D/2 pairs)
+        for (int e = threadIdx.x; e < HALF * 32; e += 256) delta[(e % HALF) * 32 + e / HALF] = p.rope[e];
         asm volatile("bar.sync 1, 256;" ::: "memory");
         int it = 0;
         bool stats_done = false;
@@ -516,30 +525,30 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             // Every epilogue warp calls prep_key_stats exactly once (here, or after the loop if it
             // left the loop early), so the named barriers inside it always match.
             if (t >= p.tiles_kv && !stats_done) {
-                prep_key_stats(p, threadIdx.x, wc);
+                prep_key_stats<D>(p, threadIdx.x, wc);
                 stats_done = true;
             }
             int m, nt;
-            prep_tile(p, t, m, nt);
+            prep_tile<D>(p, t, m, nt);
             const int n_first = m * C::BM + 128 * j + 32 * qd;
             // loads that do not depend on the accumulators are issued before waiting for them
             const bool act = n_first < p.N;
             const int nn = act ? min(n_first + lane, p.N - 1) : 0;
             const float ri = p.rinv[nn];
-            const float2 r0 = p.rope[static_cast<int64_t>(act ? n_first : 0) * 64 + lane];
-            const float2 r1 = p.rope[static_cast<int64_t>(act ? n_first : 0) * 64 + 32 + lane];
+            const float2 r0 = p.rope[static_cast<int64_t>(act ? n_first : 0) * HALF + lane];
+            const float2 r1 = HALF > 32 ? p.rope[static_cast<int64_t>(act ? n_first : 0) * HALF + 32 + lane] : r0;
             if (!mbar_wait(bar(C::B_ACC_FULL), it & 1, wc, SITE_PREP_ACC_FULL)) break;
             tc_fence_after();
             __syncwarp();  // the previous tile's reads of rbase are done
             rbase[lane] = r0;
-            rbase[32 + lane] = r1;
+            if (HALF > 32) rbase[32 + lane] = r1;
             __syncwarp();
 #pragma unroll 1
-            for (int hh = 0; hh < 2 && act; ++hh) {
-                const int col0 = nt * C::BN + 128 * hh;  // first output column of the head
-                const int sect = col0 / (p.H * 128);
-                const int h = col0 / 128 - sect * p.H;
-                prep_epilogue(p, trow + 128u * hh, sect, h, n_first, lane, ri, delta, rbase);
+            for (int hh = 0; hh < C::BN / D && act; ++hh) {
+                const int col0 = nt * C::BN + D * hh;  // first output column of the head
+                const int sect = col0 / (p.H * D);
+                const int h = col0 / D - sect * p.H;
+                prep_epilogue<D>(p, trow + static_cast<uint32_t>(D * hh), sect, h, n_first, lane, ri, delta, rbase);
             }
             tc_fence_before();
             __syncwarp();
@@ -547,7 +556,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
         // a CTA with no Q tile, or whose epilogue stopped early, still takes its share of the
         // key statistics and arrives at the grid barriers (after an abort without waiting)
-        if (!stats_done) prep_key_stats(p, threadIdx.x, wc);
+        if (!stats_done) prep_key_stats<D>(p, threadIdx.x, wc);
     }
     tc_fence_before();
     __syncthreads();
@@ -585,11 +594,12 @@ __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x
 
 int prep_smem_bytes() { return PrepCfg::SMEM_BYTES; }
 
-int launch_prep(const PrepLaunch& L)
+template <int D>
+static int launch_prep_d(const PrepLaunch& L)
 {
-    static bool attr_done = false;
+    static bool attr_done = false;  // per instantiation
     if (!attr_done) {
-        if (cudaFuncSetAttribute(fsa_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(fsa_prep_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  PrepCfg::SMEM_BYTES) != cudaSuccess)
             return -3;
         attr_done = true;
@@ -599,14 +609,21 @@ int launch_prep(const PrepLaunch& L)
     if (cudaMemsetAsync(p.gsync, 0, 3 * sizeof(unsigned), L.stream) != cudaSuccess) return -3;
     // One CTA per SM, all resident at once (the grid barriers need it; a cooperative launch
     // refuses a grid that cannot be).
-    const int total = p.tiles_kv + p.m_tiles * (p.H / 2);
+    const int total = p.tiles_kv + p.m_tiles * (p.H * D / 256);
     const int grid = total < L.sms ? total : L.sms;
     PrepParams pp = p;
     void* args[] = {const_cast<CUtensorMap*>(L.tmX), const_cast<CUtensorMap*>(L.tmW), &pp};
-    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fsa_prep_kernel), dim3(grid), dim3(kPrepThreads),
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fsa_prep_kernel<D>), dim3(grid), dim3(kPrepThreads),
                                     args, PrepCfg::SMEM_BYTES, L.stream) != cudaSuccess)
         return -3;
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_prep(const PrepLaunch& L)
+{
+    if (L.D == 128) return launch_prep_d<128>(L);
+    if (L.D == 64) return launch_prep_d<64>(L);
+    return -2;
 }
 
 }  // namespace fsa

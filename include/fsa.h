@@ -23,7 +23,7 @@
  *   lse       fp32 [H][N]   (natural log)
  *   qnorm     fp32 [H][N],  kmax fp32 [H][F],  bound fp32 [H][N],  eligible uint8 [H]
  *   x         bf16 [N][d_model] and w bf16 [3*H*D][d_model] (fsa_prep only)
- * D must be 64 or 128 (128 for fsa_prep).  H*N must stay below 2^31.
+ * D must be 64 or 128.  H*N must stay below 2^31.
  *
  * Streams: every device call is asynchronous on the given stream (a cudaStream_t
  * passed as void*; NULL = legacy default stream).  Nothing synchronises the host
@@ -225,9 +225,10 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
  *   plan's workspace;  dev_stats: optional, as in fsa_forward_ex (a bounded wait that gave
  *   up records FSA_ERR_TIMEOUT there).
  * All pointers 16-byte aligned.  Uses and may grow plan-owned workspace; the first call builds
- * the plan's rotary table (N*64 (cos, sin) pairs) on the host and uploads it.
+ * the plan's rotary table (N*D/2 (cos, sin) pairs) on the host and uploads it (again if D changes).
  * Errors: FSA_ERR_INVALID_ARG (NULL or misaligned tensor, bad d_model), FSA_ERR_UNSUPPORTED
- * (D != 128, odd H, mean-centred keys on the plan, device), FSA_ERR_CUDA.  H == 0 is a no-op.
+ * (D not 64 or 128, H*D not a multiple of 256, mean-centred keys on the plan, device),
+ * FSA_ERR_CUDA.  H == 0 is a no-op.
  */
 int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fsa_plan_t plan,
              uint16_t* q, uint16_t* k, uint16_t* v, float* qnorm, float* kmax, float* bound,

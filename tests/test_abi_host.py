@@ -173,8 +173,9 @@ def test_prep_rejects_bad_arguments_before_device_work(lib):
         def call(x=fake, w=fake, dm=256, H=2, D=128, q=fake, k=fake, v=fake):
             return lib.fsa_prep(x, w, dm, H, D, h, q, k, v, None, None, None, None, None, None)
 
-        assert call(D=64) == fsa.FSA_ERR_UNSUPPORTED          # only D = 128
-        assert call(H=3) == fsa.FSA_ERR_UNSUPPORTED           # two heads per 256-column tile
+        assert call(D=32) == fsa.FSA_ERR_UNSUPPORTED          # D = 64 or 128
+        assert call(H=3) == fsa.FSA_ERR_UNSUPPORTED           # H D a multiple of 256 (tiles of 256 columns)
+        assert call(D=64) == fsa.FSA_ERR_UNSUPPORTED          # 2 x 64 columns: half a tile
         assert call(dm=100) == fsa.FSA_ERR_INVALID_ARG        # d_model a multiple of 64
         assert call(dm=0) == fsa.FSA_ERR_INVALID_ARG
         assert call(x=None) == fsa.FSA_ERR_INVALID_ARG

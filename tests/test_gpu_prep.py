@@ -73,19 +73,22 @@ def _check_norms_consistency(res):
     assert torch.equal(res["eligible"].cpu(), el2.cpu())
 
 
-# (F, T, w, ref, block, H, d_model, seed): one full row tile; a single ragged tile; three row
-# tiles with a ragged last one and frames that do not align with 32-row blocks; T = 16
+# (F, T, w, ref, block, H, d_model, seed, D): one full row tile; a single ragged tile; three row
+# tiles with a ragged last one and frames that do not align with 32-row blocks; T = 16; and
+# D = 64 (four heads to a 256-column tile) on ragged shapes
 SMALL = [
-    (4, 64, 1, 0, 16, 2, 256, 61),
-    (3, 80, 1, 2, 80, 4, 192, 62),
-    (5, 112, 2, 0, 16, 2, 128, 63),
-    (20, 16, 3, 7, 16, 2, 64, 64),
+    (4, 64, 1, 0, 16, 2, 256, 61, 128),
+    (3, 80, 1, 2, 80, 4, 192, 62, 128),
+    (5, 112, 2, 0, 16, 2, 128, 63, 128),
+    (20, 16, 3, 7, 16, 2, 64, 64, 128),
+    (5, 112, 2, 0, 16, 4, 128, 69, 64),
+    (3, 80, 1, 2, 80, 8, 256, 70, 64),
 ]
 
 
 @pytest.mark.parametrize("case", SMALL)
 def test_prep_full_parity(dev, oracle_mod, case):
-    F, T, w_win, ref, block, H, dm, seed = case
+    F, T, w_win, ref, block, H, dm, seed, D = case
     N = F * T
     x, w = make_prep_inputs(N, dm, H, D, seed)
     res = _run_prep(dev, x, w, F, T, w_win, ref, block, H)
