@@ -150,6 +150,38 @@ def test_dense_window_is_textbook_attention(oracle_mod):
         np.testing.assert_allclose(res["lse"], logsumexp(logits, axis=-1), rtol=1e-12, atol=1e-12)
 
 
+
+def test_attention_is_invariant_to_key_order_within_frames(oracle_mod):
+    # Permuting the tokens of every frame (the same permutation for k and v) leaves each
+    # frame's key set, and so every softmax, unchanged.
+    H, F, T, D, w, ref = 2, 5, 16, 32, 1, 3
+    q, k, v = make_qkv(H, F * T, D, seed=12)
+    g = torch.Generator().manual_seed(13)
+    perm = torch.cat([f * T + torch.randperm(T, generator=g) for f in range(F)])
+    a = oracle_mod.attention_full(q, k, v, F, T, w, ref)
+    b = oracle_mod.attention_full(q, k[:, perm].contiguous(), v[:, perm].contiguous(), F, T, w, ref)
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["lse"], a["lse"], rtol=1e-13, atol=1e-13)
+
+
+def test_key_translation_moves_lse_only(oracle_mod):
+    # Adding one vector m to every key adds c <q_i, m> to every logit of row i: the softmax and
+    # out do not change, and lse moves by exactly that row constant.  Integer-valued keys keep
+    # the shifted keys exact in bf16.
+    H, F, T, D, w, ref = 2, 4, 16, 16, 1, 0
+    q, _, v = make_qkv(H, F * T, D, seed=14)
+    rng = np.random.default_rng(15)
+    z = rng.integers(-3, 4, size=(H, F * T, D)).astype(np.float32)
+    m = rng.integers(-8, 9, size=(H, 1, D)).astype(np.float32)
+    k0 = torch.tensor(z).to(torch.bfloat16)
+    k1 = torch.tensor(z + m).to(torch.bfloat16)
+    assert torch.equal(k1.float(), torch.tensor(z + m))
+    a = oracle_mod.attention_full(q, k0, v, F, T, w, ref)
+    b = oracle_mod.attention_full(q, k1, v, F, T, w, ref)
+    shift = np.einsum("hnd,hd->hn", _f64(q), m[:, 0, :].astype(np.float64)) / math.sqrt(D)
+    np.testing.assert_allclose(b["out"], a["out"], rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(b["lse"] - a["lse"], shift, rtol=1e-10, atol=1e-10)
+
 def _allowed_count(F, T, w, ref, f):
     return T * sum(1 for g in range(F) if abs(f - g) <= w or g == ref)
 
