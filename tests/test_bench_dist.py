@@ -58,3 +58,25 @@ def test_two_ranks_weak_scaling_host_logic():
     assert t0 == t1 == 15.0               # the slowest rank's time, seen by every rank
     assert v0 == v1 == pytest.approx(1e12 * 2 * 4 / 15e-3 / 1e12)
     assert r1 is None                     # the reference arm does no work off rank 0
+
+
+def test_reference_arm_prints_the_contract_line():
+    # bench.py --impl reference runs the oracle on host cores: one JSON line with the keys of
+    # the bench contract, the cpu_baseline describing this run and a zero-copy e2e
+    import json
+    import subprocess
+
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload",
+                          "tiny", "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300,
+                         cwd=ROOT, check=True).stdout
+    lines = [ln for ln in out.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 2 and d["warmup"] == 1 and d["value"] > 0
+    assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["vs_baseline"] is None
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
