@@ -318,7 +318,8 @@ def test_centred_norms_hand_derived(oracle_mod):
     #   frame 1: S = {0, 1}  Kc = 2  bound = 1*2 + (-1)*3 = -1  kbar = 1.5  gap_hat = -1 + 1.5 = 0.5
     #   frame 2: S = {0, 2}  Kc = 3  bound = 2*3 + 2*3 = 12     kbar = 3.5  gap_hat = 12 - 7 = 5
     # Row maxima: 1, -1, 12 (frames 1 and 2 meet their centred bound exactly).  Without
-    # centring the bounds are 1*1, 1*2, 2*6 and the key maxima 1, 2, 6.
+    # centring the bounds are 1*1, 1*2, 2*6, the key maxima 1, 2, 6 and the gap statistics
+    # 1 - 1, 2 + 1.5, 12 - 7.
     q = _bf16([1, -1, 2]).reshape(1, 3, 1)
     k = _bf16([1, 2, 6]).reshape(1, 3, 1)
     c = oracle_mod.norms(q, k, F=3, T=1, w=0, ref=0, scale=1.0, tau=4.5, center=True)
@@ -329,6 +330,11 @@ def test_centred_norms_hand_derived(oracle_mod):
     u = oracle_mod.norms(q, k, F=3, T=1, w=0, ref=0, scale=1.0, center=False)
     np.testing.assert_allclose(u["kmax"][0], [1.0, 2.0, 6.0], atol=1e-15)
     np.testing.assert_allclose(u["bound"][0], [1.0, 2.0, 12.0], atol=1e-15)
+    # uncentred gap statistic bound - q kbar_S: 1 - 1*1, 2 - (-1)*1.5, 12 - 2*3.5
+    np.testing.assert_allclose(u["gap_hat"][0], [0.0, 3.5, 5.0], atol=1e-15)
+    # eligible iff the worst gap statistic <= tau, the boundary included (5 is exact here)
+    for tau, elig in ((4.9, 0), (5.0, 1), (5.1, 1)):
+        assert oracle_mod.norms(q, k, F=3, T=1, w=0, ref=0, scale=1.0, tau=tau)["eligible"].tolist() == [elig]
     att = oracle_mod.attention_full(q, k, k, F=3, T=1, w=0, ref=0, scale=1.0)
     np.testing.assert_allclose(att["rowmax"][0], [1.0, -1.0, 12.0], atol=1e-15)
 
@@ -398,6 +404,11 @@ def test_prep_hand_derived_rotation(oracle_mod):
     np.testing.assert_allclose(r["v"][0, 1], [3 * s, 0, 0, 3 * s], atol=1e-15)
     np.testing.assert_allclose(r["q"][0, 0], [1, -1, 1, -1], atol=1e-15)  # rms 1, no rotation
     np.testing.assert_allclose(r["v"][0, 0], [3, -3, 3, -3], atol=1e-15)
+    # eps enters under the root: with eps = 1 token 1 has rms sqrt(8/4 + 1) = sqrt 3
+    r1 = oracle_mod.prep_full(x, w, H=1, D=4, eps=1.0, base=100.0)
+    np.testing.assert_allclose(r1["v"][0, 1], [6 / math.sqrt(3), 0, 0, 6 / math.sqrt(3)], atol=1e-15)
+    np.testing.assert_allclose(r1["v"][0, 0], [3 / math.sqrt(2), -3 / math.sqrt(2), 3 / math.sqrt(2),
+                                               -3 / math.sqrt(2)], atol=1e-15)
 
 
 def _numpy_projection(x, w, eps):
