@@ -522,7 +522,8 @@ def main():
         line["prep_roofline"] = {"bound": "tensor", "achieved": prep_flops / (prep_avg * 1e-3) / 1e12,
                                  "peak": peak, "unit": "TFLOP/s",
                                  "frac": prep_flops / (prep_avg * 1e-3) / 1e12 / peak, "ms_avg": prep_avg,
-                                 "flops": prep_flops, "kernel": "fsa_prep_kernel (K/V launch + Q launch)"}
+                                 "flops": prep_flops,
+                                 "kernel": "rms_kernel + fsa_prep_kernel (one cooperative launch) + eligibility"}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_oracle_leg(wl, target_seconds=12.0)
     plan.close()
