@@ -502,7 +502,7 @@ def main():
                    "active_flops_per_step": flops_step, "parallelism": f"independent batch per rank x{world}"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": load_traffic(),
-                     "kernel": f"fsa_attn_fwd_kernel<{D},64>", "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "kernel": f"fsa_attn_fwd_kernel<{D}> (persistent)", "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "frac_of_sustained": achieved / float(peaks.get("bf16_tflops_sustained", peak)),
                      "attention_ms_avg": attn_avg, "attention_ms_median": attn_med},
         "norms_roofline": {"bound": "hbm", "achieved": norms_bytes / (norms_avg * 1e-3) / 1e9,

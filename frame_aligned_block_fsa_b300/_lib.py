@@ -29,7 +29,7 @@ FSA_ERR_SCRATCH_LIMIT = -5
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
            "fsa_plan_set_center_keys",
            "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_prep", "fsa_norms_noalloc",
-           "fsa_status_string", "fsa_selftest_wait_timeout")
+           "fsa_last_cuda_error", "fsa_status_string", "fsa_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -75,6 +75,8 @@ def load():
             lib.fsa_prep.restype = i32
             lib.fsa_norms_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
             lib.fsa_norms_noalloc.restype = i32
+            lib.fsa_last_cuda_error.argtypes = []
+            lib.fsa_last_cuda_error.restype = i32
             lib.fsa_status_string.argtypes = [i32]
             lib.fsa_status_string.restype = ctypes.c_char_p
             lib.fsa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int32), vp]
@@ -89,7 +91,12 @@ def status_string(status: int) -> str:
 
 def _check(call: str, status: int):
     if status != FSA_OK:
-        raise FsaError(call, status)
+        err = FsaError(call, status)
+        if status == FSA_ERR_CUDA:
+            code = load().fsa_last_cuda_error()
+            err.cuda_error = code
+            err.args = (f"{err.args[0]} [CUDA error code {code}]",)
+        raise err
 
 
 def _ptr(t):
@@ -285,7 +292,8 @@ def new_stats(device):
 def read_stats(stats) -> dict:
     w32 = stats.cpu().view(__import__("torch").int32)
     return {"error": int(w32[0]), "timeout_site": int(w32[1]), "fallback_heads": int(w32[2]),
-            "underflow_rows": int(stats[2].item())}
+            "items_done": int(w32[3]), "underflow_rows": int(stats[2].item()),
+            "pairs_visited": int(stats[3].item())}
 
 
 def forward_ex(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=None, bound=None, eligible=None,

@@ -24,8 +24,6 @@ struct fsa_plan_s {
     int64_t N = 0;
     std::vector<int32_t> row_ptr, col_idx;  // block CSR
     std::vector<int32_t> runs;              // [F][kRunStride], tokens within a head
-    std::vector<int32_t> items;             // [n_items][4]
-    int n_items = 0;
     float tau = 64.0f;
     int key_tile = 0;                       // 0 = automatic
     int center_keys = 0;                    // 1: mean-centred key norms in the bound
@@ -33,7 +31,6 @@ struct fsa_plan_s {
     // device data, created on first device use
     int device = -1;
     int32_t* d_runs = nullptr;
-    int32_t* d_items = nullptr;
     // norms workspace, grown on demand (capacities in elements)
     int64_t cap_qnorm = 0, cap_bound = 0, cap_kmax = 0, cap_ksum = 0, cap_gmax = 0, cap_elig = 0;
     int64_t cap_psum = 0, cap_pmax = 0, cap_tickets = 0, cap_mu = 0, cap_htickets = 0;
@@ -72,9 +69,31 @@ struct fsa_plan_s {
 
 namespace {
 
+thread_local int g_last_cuda_error = 0;
+
+}  // namespace
+
+void fsa::note_cuda_error(int code) { g_last_cuda_error = code; }
+
+int fsa::launch_status()
+{
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return 0;
+    note_cuda_error(e);
+    return -3;
+}
+
+namespace {
+
+constexpr int kDriverErrorBase = 100000;  // driver (CUresult) codes are reported offset by this
 constexpr long long kDefaultWaitLimit = 4000000000LL;  // SM clock cycles (about 2 s)
 
-int cuda_status(cudaError_t e) { return e == cudaSuccess ? FSA_OK : FSA_ERR_CUDA; }
+int cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return FSA_OK;
+    fsa::note_cuda_error(e);
+    return FSA_ERR_CUDA;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -101,7 +120,7 @@ int upload(T** dst, const std::vector<T>& src)
     return FSA_OK;
 }
 
-// First device use: check the device and upload the key runs and the work list.
+// First device use: check the device, upload the key runs and read the SM count.
 int ensure_device(fsa_plan_s* P)
 {
     int rc = check_device();
@@ -111,7 +130,7 @@ int ensure_device(fsa_plan_s* P)
     if (P->device == dev) return FSA_OK;
     if (P->device != -1) return FSA_ERR_INVALID_ARG;  // a plan serves one device
     if ((rc = upload(&P->d_runs, P->runs)) != FSA_OK) return rc;
-    if ((rc = upload(&P->d_items, P->items)) != FSA_OK) return rc;
+    if (cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FSA_ERR_CUDA;
     P->device = dev;
     return FSA_OK;
 }
@@ -177,7 +196,9 @@ int make_tensor_map(CUtensorMap* m, const void* base, int64_t rows, int D, int b
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FSA_OK : FSA_ERR_CUDA;
+    if (r == CUDA_SUCCESS) return FSA_OK;
+    fsa::note_cuda_error(kDriverErrorBase + static_cast<int>(r));
+    return FSA_ERR_CUDA;
 }
 
 int check_shape(const fsa_plan_s* P, int H, int D)
@@ -247,25 +268,30 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
     if ((rc = make_tensor_map(&mv, v, rows, D, NK)) != FSA_OK) return rc;
     fsa::AttnLaunch L;
     L.D = D;
-    L.NK = NK;
     L.H = H;
+    L.sms = P->sms;
     L.tmQ = &mq;
     L.tmK = &mk;
     L.tmV = &mv;
     L.stream = st;
-    L.params.items = P->d_items;
-    L.params.runs = P->d_runs;
-    L.params.n_items = P->n_items;
-    L.params.N = static_cast<int>(P->N);
-    L.params.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
-    L.params.mode = mode;
-    L.params.bound = bound;
-    L.params.eligible = eligible;
-    L.params.out = out;
-    L.params.lse = lse;
-    L.params.rowmax = rowmax;
-    L.params.stats = dev_stats;
-    L.params.wait_limit = kDefaultWaitLimit;
+    fsa::AttnParams& a = L.params;
+    a.runs = P->d_runs;
+    a.F = P->F;
+    a.T = P->T;
+    a.N = static_cast<int>(P->N);
+    a.n_qt = (P->T + 127) / 128;
+    a.per_head = P->F * a.n_qt;
+    a.total = H * a.per_head;
+    a.NK = NK;
+    a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+    a.mode = mode;
+    a.bound = bound;
+    a.eligible = eligible;
+    a.out = out;
+    a.lse = lse;
+    a.rowmax = rowmax;
+    a.stats = dev_stats;
+    a.wait_limit = kDefaultWaitLimit;
     rc = fsa::launch_attention(L);
     return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
 }
@@ -286,8 +312,6 @@ int ensure_prep_workspace(fsa_plan_s* P, int H, int D)
     if ((rc = grow(&P->d_ks, &P->cap_ks, hf)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_kbar, &P->cap_kbar, hf * D)) != FSA_OK) return rc;
     if ((rc = grow(&P->d_gsync, &P->cap_gsync, int64_t(3))) != FSA_OK) return rc;
-    if (P->sms == 0 && cudaDeviceGetAttribute(&P->sms, cudaDevAttrMultiProcessorCount, P->device) != cudaSuccess)
-        return FSA_ERR_CUDA;
     if (P->d_rope == nullptr || P->rope_d != D) {
         cudaFree(P->d_rope);
         P->d_rope = nullptr;
@@ -361,6 +385,13 @@ int fsa::plan_view(const fsa_plan_s* P, PlanView* out)
 }
 
 extern "C" {
+
+int fsa_last_cuda_error(void)
+{
+    const int e = g_last_cuda_error;
+    g_last_cuda_error = 0;
+    return e;
+}
 
 const char* fsa_status_string(int status)
 {
@@ -446,35 +477,6 @@ int fsa_plan(int F, int T, int w, int ref, int block, fsa_plan_t* out)
             R[0] = n;
         }
 
-        // Work items: pairs of 128-row query tiles inside one frame (the last tile of a frame
-        // may be ragged, a frame with an odd tile count ends with a single tile).  Longest
-        // first; the kernel adds the head index on top (head-major launch order).
-        const int n_qt = (T + 127) / 128;
-        const int n_pairs = (n_qt + 1) / 2;
-        struct Item {
-            int64_t cost;
-            int f, pair;
-        };
-        std::vector<Item> order;
-        for (int f = 0; f < F; ++f) {
-            int64_t keys = 0;
-            const int32_t* R = &P->runs[static_cast<size_t>(f) * kRunStride];
-            for (int r = 0; r < R[0]; ++r) keys += R[2 + 2 * r];
-            for (int pr = 0; pr < n_pairs; ++pr) {
-                const int rows = std::min(256, T - 256 * pr);
-                order.push_back({keys * (rows > 128 ? 2 : 1), f, pr});
-            }
-        }
-        std::stable_sort(order.begin(), order.end(), [](const Item& a, const Item& b) { return a.cost > b.cost; });
-        P->n_items = static_cast<int>(order.size());
-        P->items.resize(order.size() * 4);
-        for (size_t i = 0; i < order.size(); ++i) {
-            const int r0 = 256 * order[i].pair;
-            P->items[4 * i + 0] = order[i].f;
-            P->items[4 * i + 1] = order[i].f * T + r0;
-            P->items[4 * i + 2] = std::min(128, T - r0);
-            P->items[4 * i + 3] = std::max(0, std::min(128, T - r0 - 128));
-        }
     } catch (...) {
         delete P;
         return FSA_ERR_INVALID_ARG;
@@ -492,7 +494,6 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaSetDevice(plan->device);
         cudaDeviceSynchronize();
         cudaFree(plan->d_runs);
-        cudaFree(plan->d_items);
         cudaFree(plan->d_qnorm);
         cudaFree(plan->d_bound);
         cudaFree(plan->d_kmax);
@@ -644,8 +645,8 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
     if (H == 0) return FSA_OK;  // empty problem: nothing to read or write
     if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FSA_ERR_INVALID_ARG;
-    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile(D);
-    if (NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
+    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile;
+    if (NK > fsa::kMaxKeyTile) return FSA_ERR_UNSUPPORTED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     std::lock_guard<std::mutex> lock(plan->mu);
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
@@ -668,8 +669,8 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
     if (heads_per_chunk < 0) return FSA_ERR_INVALID_ARG;
     if (H == 0) return FSA_OK;
     if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
-    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile(D);
-    if (NK > fsa::kMaxKeyTile(D)) return FSA_ERR_UNSUPPORTED;
+    const int NK = plan->key_tile ? plan->key_tile : fsa::kMaxKeyTile;
+    if (NK > fsa::kMaxKeyTile) return FSA_ERR_UNSUPPORTED;
     const int hc = heads_per_chunk ? std::min(heads_per_chunk, H) : std::max(1, (H + 7) / 8);
     const int chunks = (H + hc - 1) / hc;
     cudaStream_t caller = static_cast<cudaStream_t>(stream);

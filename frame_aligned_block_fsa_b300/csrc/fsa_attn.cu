@@ -7,41 +7,51 @@
 //    no padding of the key side and no second pass or merge;
 //  * section "Giai phong Softmax", Fig. 4: on eligible heads the running max is replaced by
 //    the per-row upper bound b_i = c ||q_i|| max ||k_j|| computed beforehand, so
-//    p = exp(s - b_i) needs no rescale of the accumulator; heads that fail the eligibility
-//    test take the running-max path inside the same kernel.
+//    p = exp(s - b_i) needs no rescale of the accumulator, and no tile depends on the one
+//    before it; heads that fail the eligibility test take the running-max path inside the
+//    same kernel.
 //
-// B300 design (one CTA per SM, 18 warps, two 128-row query tiles j = 0, 1 of one frame):
-//   warps 0-7   query tile 0: per key tile the softmax, at the end the epilogue.  A thread
-//               owns one row (= TMEM lane); the two warps of a lane quarter (w and w + 4)
-//               split the key tile's 16-column chunks (even / odd), so a row's
-//               exponentials run in two warps at once.
-//   warps 8-15  the same for query tile 1
-//   warp 16     TMA producer: the two query tiles once, then K and V tiles of up to NK keys
-//               through an NS-stage mbarrier ring (128-byte swizzled boxes)
-//   warp 17     allocates TMEM and issues tcgen05.mma (the warp runs the loop, one elected
-//               lane issues):
-//                 S_j  = Q_j K^T   (A = Q_j, B = K tile, both from shared memory)
-//                 O_j += P_j V     (A = P_j from TMEM, B = V tile from shared memory, MN-major)
+// B300 design: a persistent kernel, one CTA per SM, 16 warps.  The work list is every
+// (head, frame, 128-row query tile); CTA b takes items b, b + G, b + 2G, ... (G CTAs), in
+// head-major, frame-major order, so the CTAs that run at the same time share their heads'
+// K and V in L2.  Every role walks the same item sequence and, per item, the frame's key runs
+// in key tiles of at most NK (<= 64) keys (the last tile of a run may be narrower, a multiple
+// of 16).  A tile counter g runs over all items of the CTA.
 //
-// Each query tile has two S buffers in TMEM, so the MMAs run two key tiles ahead of the
-// softmax: S_j(t+2) is issued right after PV_j(t), into the buffer PV_j(t) has just read P_j(t)
-// from.  The softmax therefore finds S_j(t+1) ready when it finishes tile t, and the chain
-// "softmax, hand-off, MMAs, hand-off back" no longer sets the pace; the tensor pipe and the
-// exponentials do.  (The tensor pipe takes MMAs from a very short queue, so an issuing thread
-// is blocked for about as long as its MMAs take; with one S buffer per tile the pipe idled
-// for every hand-off.)  Q stays in shared memory to leave TMEM for the second buffer.
+//   warps 0-11  softmax and epilogue, in three groups of four (warps 0-3, 4-7, 8-11), one warp
+//               per TMEM lane quarter: a thread owns one query row and all keys of its group's
+//               tiles.  On norm-bound items the groups take the tiles in turn (tile t of an item
+//               goes to group t % 3), so three tiles are in the softmax at once: with a fixed bound no
+//               tile waits for the one before it.  Running-max items go to group 0 alone (each
+//               tile needs the previous tile's max), whose threads then keep the row max without
+//               any exchange.
+//   warp 12     issues the S side (the warp runs the loop, one elected lane issues):
+//                 Q(item)  -> TMEM by tcgen05.cp from shared memory (two Q slots, so the copy
+//                             for the next item never touches the one in use)
+//                 S(g)     = Q K(g)^T      A = Q from TMEM, B = K tile from shared memory
+//   warp 13     issues the PV side:
+//                 O       += P(g) V(g)     A = P from TMEM, B = V tile from shared memory
+//               (the pipe takes an MMA only when it has room, so an issuing thread is held for
+//               about as long as its MMAs run; with two issuers one does its bookkeeping while
+//               the other feeds the pipe)
+//   warps 14-15 TMA producers, one for Q and K, one for V: K(g) and V(g) go to slot g & 3 of a K
+//               and a V ring (the slots of S buffer g & 3), each item's Q tile into its own
+//               staging buffer.
 //
-// TMEM (512 columns): per query tile j a 256-column region
-//   [S_j buffer 0: NK fp32][S_j buffer 1: NK fp32][O_j: D fp32].
-// P_j(t) overwrites S_j(t) in its buffer after the softmax has read it: the 8 bf16-pair
-// columns of the 16 keys of S chunk c go to the first 8 columns of that chunk, so each warp
-// overwrites only columns it has read itself.  S_j(t+2) is issued after PV_j(t) by the same
-// thread, and the tensor pipe executes one thread's MMAs in issue order, so PV_j(t) has read
-// P_j(t) before S_j(t+2) overwrites it.
+// Tensor work: S has four TMEM buffers (tile g uses buffer g & 3), so while the softmax turns
+// S(g) into P(g) the pipe has the three following S tiles and three PV products to compute.
+// PV(g) is issued once P(g) is in TMEM; S(g + 4) goes into the same buffer once PV(g) is done
+// (a commit of the PV issuer frees the buffer).
 //
-// Key tiles: each key run (a whole number of frames) is cut into tiles of NK keys and one
-// last narrower tile of the remaining len mod NK keys (a multiple of 16, since T is).  Every
-// tile is fully inside the mask; a narrower tile is an MMA of smaller N (S) or K (PV).
+// One O accumulator: the epilogue of item k (O / l -> out) runs in all twelve softmax warps
+// when the tile walk reaches item k + 1 (the group that owns item k + 1's first tile first
+// produces its P), while the pipe computes S of item k + 1; the first PV of item k + 1 waits
+// until the epilogue has read O out of TMEM.
+//
+// TMEM (512 columns): [Q slot 0: D/2][Q slot 1: D/2][S buffers 0-3: 64 each][O: D].
+// P(g) overwrites S(g) in its buffer after the softmax has read it: the 8 bf16-pair columns of
+// the 16 keys of chunk c go to the first 8 columns of that chunk, so each warp overwrites only
+// columns it has read itself.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -52,70 +62,71 @@
 
 namespace fsa {
 
-constexpr int kAttnThreads = 576;  // 16 softmax warps, the TMA warp, the MMA warp
-constexpr int kWarpTma = 16, kWarpMma = 17;
+constexpr int kGroups = 3;                  // softmax warp groups (tiles round-robin)
+constexpr int kGroupWarps = 4;              // one warp per lane quarter
+constexpr int kSoftWarps = kGroups * kGroupWarps;  // 12
+constexpr int kAttnThreads = 32 * (kSoftWarps + 4);  // + two tcgen05 issuers and two TMA warps
+constexpr int kWarpS = kSoftWarps, kWarpPV = kSoftWarps + 1, kWarpTmaK = kSoftWarps + 2, kWarpTmaV = kSoftWarps + 3;
+constexpr int kNBuf = 4;                    // S buffers
+constexpr int kBufCols = 64;                // TMEM columns (= keys) of an S buffer
+// Frames whose key runs are copied to shared memory when the kernel starts; larger plans
+// read them from global memory.
+constexpr int kSmemRunFrames = 256;
 
-template <int D, int NK>
+template <int D>
 struct AttnCfg {
     static_assert(D == 64 || D == 128, "head dim");
-    static_assert(NK % 16 == 0 && NK >= 16 && NK <= kMaxKeyTile(D), "key tile");
-    static constexpr int BM = 128;                      // query rows per tile (MMA M)
-    static constexpr int PANELS = D / 64;               // 64-element (128 B) swizzle panels
-    static constexpr int Q_PANEL_BYTES = BM * 128;
-    static constexpr int Q_TILE_BYTES = BM * D * 2;
-    static constexpr int KV_PANEL_BYTES = NK * 128;
-    static constexpr int KV_TILE_BYTES = NK * D * 2;
-    static constexpr int STAGE_BYTES = 2 * KV_TILE_BYTES;  // K and V
-    static constexpr int SMEM_LIMIT = 232448;              // max dynamic smem per block
-    static constexpr int RESERVED = 256;                   // barriers + flags
-    static constexpr int LSUM_BYTES = 2 * 2 * 128 * 4;     // row-sum halves (epilogue)
-    static constexpr int NS_FIT =
-        (SMEM_LIMIT - 1024 - RESERVED - LSUM_BYTES - 2 * 2 * 2 * 128 * 4 - 2 * Q_TILE_BYTES) / STAGE_BYTES;
-    static constexpr int NS = NS_FIT < 6 ? NS_FIT : 6;
-    static_assert(NS >= 3, "pipeline depth: two key tiles ahead of the one being read");
+    static constexpr int PANELS = D / 64;              // 64-element (128 B) swizzle panels of a row
+    static constexpr int KV_PANEL = kBufCols * 128;    // 64 rows x 128 B
+    static constexpr int SLOT_BYTES = PANELS * KV_PANEL;  // one K or V tile of up to 64 rows
+    static constexpr int Q_PANEL = 128 * 128;          // 128 rows x 128 B
+    static constexpr int Q_BYTES = PANELS * Q_PANEL;
+    // K(g) and V(g) go to slot g & 3 of a K and a V ring, the slots of S buffer g & 3: the
+    // commit that ends S(g) frees K slot g & 3, the one that ends PV(g) frees V slot g & 3.
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = 2 * Q_TILE_BYTES;
-    static constexpr int V_OFF = K_OFF + NS * KV_TILE_BYTES;
-    static constexpr int BAR_OFF = V_OFF + NS * KV_TILE_BYTES;
+    static constexpr int K_OFF = Q_BYTES;
+    static constexpr int V_OFF = K_OFF + kNBuf * SLOT_BYTES;
+    static constexpr int BAR_OFF = V_OFF + kNBuf * SLOT_BYTES;
     // barrier indices
-    static constexpr int B_QFULL = 0;
-    static constexpr int B_KVFULL = 1;                // NS: K and V of a stage landed
-    static constexpr int B_KVEMPTY = B_KVFULL + NS;   // NS: the MMAs reading a stage are done
-    static constexpr int B_SFULL = B_KVEMPTY + NS;    // 4: S_j in buffer b complete (index 2 j + b)
-    static constexpr int B_PVDONE = B_SFULL + 4;      // 2: PV_j complete
-    // 4: P_j of a key tile in buffer b in TMEM (index 2 j + b, 8 arrivals).  One barrier per
-    // buffer: the softmax can finish key tile t+1 before the MMA warp has waited for tile t,
-    // but never tile t+2, so each barrier is at most one phase ahead of its waiter.
-    static constexpr int B_PFULL = B_PVDONE + 2;
-    static constexpr int B_DRAIN = B_PFULL + 4;
-    static constexpr int N_BARS = B_DRAIN + 1;
-    // abort flag (+0), TMEM address (+8), row-sum exchange counters (+16, +20), row-max
-    // exchange counters per (query tile, lane quarter) (+24 .. +56)
-    static constexpr int MISC_OFF = BAR_OFF + N_BARS * 8;
-    static_assert(MISC_OFF + 56 <= BAR_OFF + RESERVED, "reserved area");
-    // per query tile, per column half, per row: the half's partial row sum (epilogue)
-    static constexpr int LSUM_OFF = BAR_OFF + RESERVED;
-    // per key-tile parity, query tile, column half, row: the half's tile max (running-max path)
-    static constexpr int MMAX_OFF = LSUM_OFF + LSUM_BYTES;
-    static constexpr int MMAX_BYTES = 2 * 2 * 2 * 128 * 4;
-    static constexpr int SMEM_USED = 1024 + MMAX_OFF + MMAX_BYTES;
-    // At least half of the SM's shared memory, so two CTAs never share an SM and contend for
-    // its 512 TMEM columns.
-    static constexpr int SMEM_BYTES = SMEM_USED > 120 * 1024 ? SMEM_USED : 120 * 1024;
-    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory");
-    static_assert(KV_PANEL_BYTES % 1024 == 0, "swizzle atoms must stay 1024-byte aligned");
+    static constexpr int B_KFULL = 0;                  // kNBuf: K slot b landed
+    static constexpr int B_VFULL = kNBuf;              // kNBuf: V slot b landed
+    static constexpr int B_QFULL = 2 * kNBuf;          // the staged Q tile landed
+    static constexpr int B_QEMPTY = B_QFULL + 1;       // its copy into TMEM is done
+    static constexpr int B_SFULL = B_QEMPTY + 1;       // kNBuf: S in buffer b complete (K slot b free)
+    static constexpr int B_PFULL = B_SFULL + kNBuf;    // kNBuf: P in buffer b written (one group's warps)
+    static constexpr int B_PVDONE = B_PFULL + kNBuf;   // PV of a running-max tile done (not the item's last)
+    static constexpr int B_OFULL = B_PVDONE + 1;       // the last PV of an item done: O final
+    static constexpr int B_OFREE = B_OFULL + 1;        // the epilogue has read O (all softmax warps)
+    static constexpr int B_BFREE = B_OFREE + 1;        // kNBuf: PV of buffer b's tile done (S buffer b and V
+                                                       // slot b free)
+    static constexpr int B_QDONE = B_BFREE + kNBuf;    // 2: the last S MMA of an item using Q slot s done
+    static constexpr int B_DRAIN = B_QDONE + 2;        // 2: everything an issuer issued is done
+    static constexpr int N_BARS = B_DRAIN + 2;
+    // abort flag (+0), TMEM address (+4), per lane quarter: row-sum exchange counters (+8 .. +24)
+    static constexpr int MISC_OFF = BAR_OFF + 8 * N_BARS;
+    static constexpr int MISC_BYTES = 32;
+    // per item parity, group, row: a group's part of the row sum (epilogue)
+    static constexpr int LSUM_OFF = (MISC_OFF + MISC_BYTES + 15) & ~15;
+    static constexpr int LSUM_BYTES = 2 * kGroups * 128 * 4;
+    static constexpr int RUNS_OFF = LSUM_OFF + LSUM_BYTES;
+    static constexpr int SMEM_USED = RUNS_OFF + kSmemRunFrames * kRunStride * 4;
+    // room to align the buffers to 1024 B, and at least half of the SM's shared memory, so two
+    // CTAs never share an SM (each takes all 512 TMEM columns)
+    static constexpr int SMEM_BYTES = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(SMEM_BYTES > 116 * 1024, "one CTA per SM: its 512 TMEM columns are not shared");
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t REGION = 256;
-    static_assert(2 * NK + D <= static_cast<int>(REGION), "TMEM budget");
-    static constexpr uint32_t t_s(int j, int b) { return REGION * j + NK * b; }  // chunk c's P at + 16 c
-    static constexpr uint32_t t_o(int j) { return REGION * j + 2 * NK; }
+    static constexpr uint32_t t_q(int s) { return static_cast<uint32_t>(s * (D / 2)); }
+    static constexpr uint32_t t_s(int b) { return static_cast<uint32_t>(D + kBufCols * b); }
+    static constexpr uint32_t T_O = static_cast<uint32_t>(D + kBufCols * kNBuf);
+    static_assert(D + kBufCols * kNBuf + D <= 512, "TMEM budget");
     static constexpr uint32_t IDESC_O = idesc_bf16_f32(128, D, false, true);
 };
 
 // wait sites (diagnostic codes in fsa_stats_t::timeout_site)
 enum : int {
-    SITE_PROD_EMPTY = 1, SITE_MMA_Q = 2, SITE_MMA_K = 3, SITE_MMA_P = 6, SITE_SOFT_S = 7, SITE_SOFT_O = 8,
-    SITE_DRAIN = 9, SITE_SELFTEST = 10
+    SITE_PROD_EMPTY = 1, SITE_PROD_Q = 2, SITE_MMA_SLOT = 3, SITE_MMA_OFREE = 4, SITE_MMA_Q = 5, SITE_MMA_P = 6,
+    SITE_SOFT_S = 7, SITE_SOFT_O = 8, SITE_DRAIN = 9, SITE_SELFTEST = 10, SITE_SOFT_X = 11
 };
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -123,100 +134,164 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kFltMin = 1.17549435e-38f;
 constexpr float kUnderflowGap = 87.33654475055310898657f;  // 126 ln 2
 
-// Loads `W` columns (W % 16 == 0) of this thread's TMEM lane into v (waits).
-template <int W>
-__device__ __forceinline__ void tmem_load_cols(uint32_t taddr, float* v)
-{
-#pragma unroll
-    for (int c = 0; c < W / 16; ++c) tmem_ld_x16(taddr + 16 * c, v + 16 * c);
-    tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < W; ++i) reg_fence(v[i]);
-}
+// The key tiles of one CTA's items, in order.  An item is one 128-row query tile (h, f, qt);
+// its keys are the runs of frame f (at most two: the window and the reference frame when it
+// lies outside the window), cut into tiles of at most NK keys.  The kernel parameters are
+// passed to every call instead of being held, so the iterator costs registers only for its
+// position.
+struct TileIter {
+    int it;                          // current item index
+    int local = -1;                  // items of this CTA begun so far, minus one
+    int h = 0, row0 = 0, valid = 0;  // current item: head, first query token, valid rows
+    int s0 = 0, l0 = 0, s1 = 0, lt = 0, pos = 0;  // runs (lt = total keys) and position
 
-// Walks a query frame's key runs in tiles of at most NK keys: (first key, width).  The runs
-// (at most kMaxRuns) are read once into registers, so that stepping costs no memory access.
-template <int NK>
-struct KeyTiles {
-    int s0 = 0, s1 = 0, s2 = 0, s3 = 0, l0 = 0, l1 = 0, l2 = 0, l3 = 0;
-    int r = 0, k0 = 0;
-    __device__ explicit KeyTiles(const int32_t* rr)
+    __device__ TileIter() : it(static_cast<int>(blockIdx.x) - static_cast<int>(gridDim.x)) {}
+
+    __device__ __forceinline__ bool load(const AttnParams& p, const int32_t* runs_tab)
     {
-        static_assert(kMaxRuns == 4, "one register pair per run");
-        const int n = rr[0];
-        s0 = rr[1];
-        l0 = rr[2];
-        if (n > 1) { s1 = rr[3]; l1 = rr[4]; }
-        if (n > 2) { s2 = rr[5]; l2 = rr[6]; }
-        if (n > 3) { s3 = rr[7]; l3 = rr[8]; }
+        it += static_cast<int>(gridDim.x);
+        if (it >= p.total) {
+            lt = pos = 0;
+            return false;
+        }
+        ++local;
+        h = it / p.per_head;
+        const int loc = it - h * p.per_head;
+        const int f = loc / p.n_qt;
+        const int qt = loc - f * p.n_qt;
+        row0 = f * p.T + qt * 128;
+        valid = min(128, p.T - qt * 128);
+        const int32_t* R = runs_tab + f * kRunStride;
+        const int nr = R[0];
+        s0 = R[1];
+        l0 = R[2];
+        s1 = nr > 1 ? R[3] : 0;
+        lt = l0 + (nr > 1 ? R[4] : 0);
+        pos = 0;
+        return true;
     }
-    __device__ __forceinline__ void next(int& start, int& width)
+
+    // The next tile: first key (token within the head), width, first / last tile of its item.
+    __device__ __forceinline__ bool next(const AttnParams& p, const int32_t* runs_tab, int& start, int& width,
+                                         bool& first, bool& last)
     {
-        const int len = r == 0 ? l0 : (r == 1 ? l1 : (r == 2 ? l2 : l3));
-        const int base = r == 0 ? s0 : (r == 1 ? s1 : (r == 2 ? s2 : s3));
-        start = base + k0;
-        width = min(NK, len - k0);
-        k0 += width;
-        if (k0 == len) {
-            k0 = 0;
-            ++r;
+        if (pos == lt && !load(p, runs_tab)) return false;
+        first = pos == 0;
+        if (pos < l0) {
+            start = s0 + pos;
+            width = min(p.NK, l0 - pos);
+        } else {
+            start = s1 + (pos - l0);
+            width = min(p.NK, lt - pos);
+        }
+        pos += width;
+        last = pos == lt;
+        return true;
+    }
+};
+
+// Bounded waits of the attention kernel.  The abort flag lives in shared memory and the limit and
+// error words come from the kernel parameters, so a waiter keeps nothing in registers for them.
+// A waiter that gives up raises the abort flag and records FSA_ERR_TIMEOUT and its site.
+struct AttnWait {
+    uint32_t abort_addr;
+
+    __device__ __forceinline__ bool aborted() const
+    {
+        uint32_t v;
+        asm volatile("ld.volatile.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(abort_addr) : "memory");
+        return v != 0;
+    }
+    __device__ __noinline__ void fail(const AttnParams& p, int site) const
+    {
+        asm volatile("st.volatile.shared::cta.u32 [%0], %1;" ::"r"(abort_addr), "r"(1u) : "memory");
+        if (p.stats) {
+            atomicCAS(&p.stats->error, 0, -4 /* FSA_ERR_TIMEOUT */);
+            atomicCAS(&p.stats->timeout_site, 0, site);
+        }
+    }
+    // wait for the phase of the given parity of mbarrier `b`
+    __device__ __forceinline__ bool bar(const AttnParams& p, uint32_t b, uint32_t parity, int site,
+                                        bool honour_abort = true) const
+    {
+        if (mbar_test_wait(b, parity)) return true;
+        const long long t0 = clock64();
+        while (true) {
+            if (mbar_try_wait(b, parity)) return true;
+            if (honour_abort && aborted()) return false;
+            if (clock64() - t0 > p.wait_limit) {
+                fail(p, site);
+                return false;
+            }
+        }
+    }
+    // wait until the shared counter at `addr` reaches `target`
+    __device__ __forceinline__ bool counter(const AttnParams& p, uint32_t addr, uint32_t target, int site) const
+    {
+        if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
+        const long long t0 = clock64();
+        uint32_t nap = 16;
+        while (true) {
+            if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
+            __nanosleep(nap);
+            nap = min(nap * 2u, 256u);
+            if (aborted()) return false;
+            if (clock64() - t0 > p.wait_limit) {
+                fail(p, site);
+                return false;
+            }
         }
     }
 };
 
-template <int D, int NK>
+template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p)
 {
-    using C = AttnCfg<D, NK>;
+    using C = AttnCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_u32 = smem_u32(smem_raw);
     const uint32_t sbase = (raw_u32 + 1023u) & ~1023u;
     uint8_t* sgen = smem_raw + (sbase - raw_u32);
     auto bar = [&](int i) -> uint32_t { return sbase + C::BAR_OFF + 8u * static_cast<uint32_t>(i); };
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(sgen + C::MISC_OFF);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
-    uint32_t* xcount = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 16);
-    // xcount[j] counts the row-sum halves of query tile j written to shared memory
-    auto xcount_addr = [&](int j) -> uint32_t { return sbase + C::MISC_OFF + 16u + 4u * static_cast<uint32_t>(j); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 4);
+    uint32_t* counters = reinterpret_cast<uint32_t*>(sgen + C::MISC_OFF + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int h = blockIdx.x / p.n_items;
-    const int item = blockIdx.x - h * p.n_items;
-    const int4 it = reinterpret_cast<const int4*>(p.items)[item];
-    const int f = it.x, q_row0 = it.y, valid0 = it.z, valid1 = it.w;
-    const int nq = valid1 > 0 ? 2 : 1;
-    const int32_t* runs = p.runs + f * kRunStride;
-    const int n_runs = runs[0];
-    int n_tiles = 0;
-    for (int r = 0; r < n_runs; ++r) n_tiles += (runs[2 + 2 * r] + NK - 1) / NK;
-    const int64_t head_row0 = static_cast<int64_t>(h) * p.N;
 
-    const bool use_bound = (p.mode == 0) && (p.bound != nullptr) &&
-                           (p.eligible == nullptr || p.eligible[h] != 0);
+    // key runs of every frame into shared memory when they fit
+    const bool runs_in_smem = p.F <= kSmemRunFrames;
+    int32_t* runs_s = reinterpret_cast<int32_t*>(sgen + C::RUNS_OFF);
+    if (runs_in_smem)
+        for (int i = threadIdx.x; i < p.F * kRunStride; i += blockDim.x) runs_s[i] = p.runs[i];
+    const int32_t* runs_tab = runs_in_smem ? runs_s : p.runs;
 
     if (threadIdx.x == 0) {
+        for (int b = 0; b < kNBuf; ++b) {
+            mbar_init(bar(C::B_KFULL + b), 1);
+            mbar_init(bar(C::B_VFULL + b), 1);
+        }
         mbar_init(bar(C::B_QFULL), 1);
-        for (int s = 0; s < C::NS; ++s) {
-            mbar_init(bar(C::B_KVFULL + s), 1);
-            mbar_init(bar(C::B_KVEMPTY + s), 1);
+        mbar_init(bar(C::B_QEMPTY), 1);
+        for (int b = 0; b < kNBuf; ++b) {
+            mbar_init(bar(C::B_SFULL + b), 1);
+            mbar_init(bar(C::B_PFULL + b), kGroupWarps);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(bar(C::B_SFULL + i), 1);
-        for (int i = 0; i < 8; ++i) xcount[2 + i] = 0;
-        for (int j = 0; j < 2; ++j) {
-            mbar_init(bar(C::B_PVDONE + j), 1);
-            mbar_init(bar(C::B_PFULL + 2 * j), 8);  // one arrival per softmax warp of the tile
-            mbar_init(bar(C::B_PFULL + 2 * j + 1), 8);
-            xcount[j] = 0;
+        mbar_init(bar(C::B_PVDONE), 1);
+        mbar_init(bar(C::B_OFULL), 1);
+        mbar_init(bar(C::B_OFREE), kSoftWarps);
+        for (int b = 0; b < kNBuf; ++b) mbar_init(bar(C::B_BFREE + b), 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(C::B_QDONE + i), 1);
+            mbar_init(bar(C::B_DRAIN + i), 1);
         }
-        mbar_init(bar(C::B_DRAIN), 1);
-        *abort_flag = 0;
+        for (int i = 0; i < 4; ++i) counters[i] = 0;
+        *reinterpret_cast<volatile int*>(sgen + C::MISC_OFF) = 0;  // abort flag
         fence_mbar_init();
-        if (p.stats && item == 0 && p.mode == 0 && !use_bound) atomicAdd(&p.stats->fallback_heads, 1);
     }
-    if (warp == kWarpMma) {
+    if (warp == kWarpS) {
         tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
         tmem_relinquish();
     }
@@ -225,353 +300,461 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tc_fence_after();
     const uint32_t tbase = *tmem_slot;
 
-    WaitCtl wc;
-    wc.abort = abort_flag;
-    wc.err_word = p.stats ? &p.stats->error : nullptr;
-    wc.err_site = p.stats ? &p.stats->timeout_site : nullptr;
-    wc.limit = p.wait_limit;
+    const AttnWait wt{sbase + C::MISC_OFF};
 
-    if (warp == kWarpTma) {
-        // ------------------------------------------------------------- TMA producer
+    auto kslot = [&](int b) -> uint32_t { return sbase + C::K_OFF + b * C::SLOT_BYTES; };
+    auto vslot = [&](int b) -> uint32_t { return sbase + C::V_OFF + b * C::SLOT_BYTES; };
+
+    if (warp == kWarpTmaK || warp == kWarpTmaV) {
+        // ------------------------------------------------------------- TMA producers
+        // One warp loads Q and K, the other V, each waiting only on the barriers of its own
+        // stream.  Rows past the tensor are zero-filled; rows past a narrower tile are loaded but
+        // never read.
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
+            const bool is_k = warp == kWarpTmaK;
+            tma_prefetch_desc(is_k ? &tmK : &tmV);
+            if (is_k) tma_prefetch_desc(&tmQ);
             const uint64_t pol_kv = policy_evict_last();
-            // Both query tiles in full (rows past the tensor are zero-filled; rows past the
-            // frame are computed but never stored).
-            mbar_arrive_expect_tx(bar(C::B_QFULL), static_cast<uint32_t>(nq * C::Q_TILE_BYTES));
-            for (int j = 0; j < nq; ++j)
+            const uint64_t pol_q = policy_evict_first();
+            const uint32_t kv_bytes = static_cast<uint32_t>(p.NK * D * 2);
+            const CUtensorMap* map = is_k ? &tmK : &tmV;
+            const uint32_t ring = is_k ? sbase + C::K_OFF : sbase + C::V_OFF;
+            const int b_full = is_k ? C::B_KFULL : C::B_VFULL;
+            // a slot is free once the tensor work that read it is done: S(g - 4) for K slot g & 3,
+            // PV(g - 4) for V slot g & 3
+            const int b_free = is_k ? C::B_SFULL : C::B_BFREE;
+            TileIter it;
+            int n = 0, nq = 0;  // tiles and Q tiles issued
+            int start, width;
+            bool first, last;
+            while (it.next(p, runs_tab, start, width, first, last)) {
+                const int hrow = it.h * p.N;
+                if (is_k && first) {
+                    // the item's Q tile, once the previous one has been copied into TMEM
+                    if (!wt.bar(p, bar(C::B_QEMPTY), (nq & 1) ^ 1, SITE_PROD_Q)) break;
+                    mbar_arrive_expect_tx(bar(C::B_QFULL), static_cast<uint32_t>(C::Q_BYTES));
+                    for (int pn = 0; pn < C::PANELS; ++pn)
+                        tma_load_2d_hint(sbase + C::Q_OFF + pn * C::Q_PANEL, &tmQ, pn * 64, hrow + it.row0,
+                                         bar(C::B_QFULL), pol_q);
+                    ++nq;
+                }
+                const int b = n & (kNBuf - 1);
+                if (n >= kNBuf && !wt.bar(p, bar(b_free + b), ((n >> 2) & 1) ^ 1, SITE_PROD_EMPTY)) break;
+                mbar_arrive_expect_tx(bar(b_full + b), kv_bytes);
                 for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_2d(sbase + C::Q_OFF + j * C::Q_TILE_BYTES + pn * C::Q_PANEL_BYTES, &tmQ, pn * 64,
-                                static_cast<int>(head_row0 + q_row0 + j * 128), bar(C::B_QFULL));
-            KeyTiles<NK> tiles(runs);
-            int t = 0;
-            for (; t < n_tiles; ++t) {
-                const int st = t % C::NS;
-                if (!mbar_wait(bar(C::B_KVEMPTY + st), ((t / C::NS) & 1) ^ 1, wc, SITE_PROD_EMPTY)) break;
-                int start, width;
-                tiles.next(start, width);
-                // A narrower last tile still loads a full box: the rows past it are never read
-                // by the MMAs (rows past the tensor are zero-filled).
-                const int row = static_cast<int>(head_row0 + start);
-                mbar_arrive_expect_tx(bar(C::B_KVFULL + st), 2 * C::KV_TILE_BYTES);
-                for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_2d_hint(sbase + C::K_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES, &tmK,
-                                     pn * 64, row, bar(C::B_KVFULL + st), pol_kv);
-                for (int pn = 0; pn < C::PANELS; ++pn)
-                    tma_load_2d_hint(sbase + C::V_OFF + st * C::KV_TILE_BYTES + pn * C::KV_PANEL_BYTES, &tmV,
-                                     pn * 64, row, bar(C::B_KVFULL + st), pol_kv);
+                    tma_load_2d_hint(ring + b * C::SLOT_BYTES + pn * C::KV_PANEL, map, pn * 64, hrow + start,
+                                     bar(b_full + b), pol_kv);
+                ++n;
             }
             // Every copy this thread issued must land before the CTA may exit.
-            mbar_wait(bar(C::B_QFULL), 0, wc, SITE_DRAIN, false);
-            for (int u = (t > C::NS ? t - C::NS : 0); u < t; ++u)
-                mbar_wait(bar(C::B_KVFULL + u % C::NS), (u / C::NS) & 1, wc, SITE_DRAIN, false);
+            if (nq > 0) wt.bar(p, bar(C::B_QFULL), (nq - 1) & 1, SITE_DRAIN, false);
+            for (int u = n > kNBuf ? n - kNBuf : 0; u < n; ++u)
+                wt.bar(p, bar(b_full + (u & (kNBuf - 1))), (u >> 2) & 1, SITE_DRAIN, false);
         }
-    } else if (warp == kWarpMma) {
-        // ------------------------------------------------------------- MMA issuer
-        // Prologue: S_j(0) into buffer 0 and S_j(1) into buffer 1 of every query tile j.  Per
-        // key tile t, for j = 0, 1: once softmax j has put P_j(t) into buffer t % 2, PV_j(t),
-        // then S_j(t+2) into the same buffer (the pipe runs one thread's MMAs in order).
-        // PVDONE_j is committed after every PV on running-max heads (the softmax rescales O_j
-        // only once PV_j(t-1) is done) and after the last PV on norm-bound heads.
-        //
-        // The whole warp runs this loop, so the waits and the descriptor arithmetic stay
-        // warp-uniform; one elected lane issues every tcgen05.mma and tcgen05.commit (a commit
-        // tracks the MMAs of its own thread, so the same lane issues all of them).
+    } else if (warp == kWarpS) {
+        // ------------------------------------------------------------- tcgen05 issuer: Q, S
+        // The whole warp runs the loop, so the waits stay warp-uniform; one elected lane issues
+        // every tcgen05 instruction (a commit tracks the work of its own thread).  The tests of
+        // the next tile's barriers go out right after the first MMA of a tile, so their answers
+        // are back while the pipe still has that tile's MMAs to run.
         const bool leader = elect_one();
-        // Descriptor bases; moving the start address by b bytes adds b >> 4 to the descriptor.
-        const uint64_t dq = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
-        const uint64_t dk = smem_desc_sw128(sbase + C::K_OFF, 16, 1024);
-        const uint64_t dv = smem_desc_sw128(sbase + C::V_OFF, C::KV_PANEL_BYTES, 1024);
-        // S_j = Q_j K^T into buffer buf; `probe` runs after the first MMA is queued, so that the
-        // answer of an mbarrier test it issues is back by the time the group is queued.
-        auto issue_s = [&](int j, int buf, int st, int width, auto&& probe) {
-            const uint64_t a0 = dq + static_cast<uint64_t>((j * C::Q_TILE_BYTES) >> 4);
-            const uint64_t b0 = dk + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
-            const uint32_t idesc = idesc_bf16_f32(128, width, false, false);
+        TileIter si;
+        int nq = 0;  // Q tiles copied into TMEM
+        bool ok = true;
+        int start, width;
+        bool first, last;
+        bool more = si.next(p, runs_tab, start, width, first, last);
+        bool k_seen = false, b_seen = true;  // readiness of tile x, tested ahead
+        for (int x = 0; ok && more; ++x) {
+            const int buf = x & (kNBuf - 1);
+            const int qs = si.local & 1;
+            const bool t_last = last;
+            if (first) {
+                // the Q slot was last read by item local - 2, whose last S must be done
+                if (si.local >= 2 &&
+                    !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_QDONE + qs), ((si.local >> 1) & 1) ^ 1,
+                                                          SITE_MMA_Q))))
+                    break;
+                if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_QFULL), nq & 1, SITE_MMA_Q)))) break;
+                tc_fence_after();
+                const uint64_t d0 = smem_desc_sw128(sbase + C::Q_OFF, 16, 1024);
+                if (leader) {
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                if (ks == 1) probe();
-                // 16 bf16 = 32 B inside the 128 B swizzle row; a new 64-column panel every 4 steps
-                const uint32_t qo = ((ks >> 2) * C::Q_PANEL_BYTES + (ks & 3) * 32) >> 4;
-                const uint32_t ko = ((ks >> 2) * C::KV_PANEL_BYTES + (ks & 3) * 32) >> 4;
-                if (leader) mma_ss(tbase + C::t_s(j, buf), a0 + qo, b0 + ko, idesc, ks > 0 ? 1u : 0u);
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        tmem_cp_128x256b(tbase + C::t_q(qs) + ks * 8,
+                                         d0 + static_cast<uint64_t>(((ks >> 2) * C::Q_PANEL + (ks & 3) * 32) >> 4));
+                    tc_commit(bar(C::B_QEMPTY));
+                }
+                ++nq;
             }
-            if (leader) tc_commit(bar(C::B_SFULL + 2 * j + buf));
-            __syncwarp();
-        };
-        auto no_probe = [] {};
-        auto issue_pv = [&](int j, int buf, int st, int width, bool first, bool commit) {
-            const uint64_t b0 = dv + static_cast<uint64_t>((st * C::KV_TILE_BYTES) >> 4);
+            // S(x) overwrites the buffer of tile x - 4, whose PV must be done; K(x) must be in
+            if (!__all_sync(0xffffffffu, b_seen) &&
+                !(ok = __all_sync(0xffffffffu,
+                                  wt.bar(p, bar(C::B_BFREE + buf), ((x >> 2) & 1) ^ 1, SITE_MMA_P))))
+                break;
+            if (!__all_sync(0xffffffffu, k_seen) &&
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_KFULL + buf), (x >> 2) & 1, SITE_MMA_SLOT))))
+                break;
+            tc_fence_after();
+            const uint64_t b0 = smem_desc_sw128(kslot(buf), 16, 1024);
+            const uint32_t idesc = idesc_bf16_f32(128, width, false, false);
+            const uint32_t tq = tbase + C::t_q(qs);
+            if (leader) mma_ts(tbase + C::t_s(buf), tq, b0, idesc, 0u);
+            {
+                const int xn = x + 1, bn = xn & (kNBuf - 1);
+                k_seen = mbar_test_wait(bar(C::B_KFULL + bn), (xn >> 2) & 1);
+                b_seen = xn < kNBuf || mbar_test_wait(bar(C::B_BFREE + bn), ((xn >> 2) & 1) ^ 1);
+            }
             if (leader) {
 #pragma unroll
-                for (int ks = 0; ks < NK / 16; ++ks)
-                    if (ks < width / 16)
-                        mma_ts(tbase + C::t_o(j), tbase + C::t_s(j, buf) + ks * 16, b0 + ((ks * 16 * 128) >> 4),
-                               C::IDESC_O, (!first || ks > 0) ? 1u : 0u);
-                if (commit) tc_commit(bar(C::B_PVDONE + j));
+                for (int ks = 1; ks < D / 16; ++ks)
+                    mma_ts(tbase + C::t_s(buf), tq + ks * 8,
+                           b0 + static_cast<uint64_t>(((ks >> 2) * C::KV_PANEL + (ks & 3) * 32) >> 4), idesc, 1u);
+                tc_commit(bar(C::B_SFULL + buf));
+                if (t_last) tc_commit(bar(C::B_QDONE + qs));
             }
             __syncwarp();
-        };
-        // An mbarrier test answers only after a long round trip while shared memory is busy,
-        // so readiness is tested early (the answer `seen`) and waited for only when it was no.
-        auto stage_test = [&](int t) { return mbar_test_wait(bar(C::B_KVFULL + t % C::NS), (t / C::NS) & 1); };
-        auto stage_wait = [&](int t, bool seen) -> bool {
-            if (__all_sync(0xffffffffu, seen)) return true;
-            return __all_sync(0xffffffffu, mbar_wait(bar(C::B_KVFULL + t % C::NS), (t / C::NS) & 1, wc, SITE_MMA_K));
-        };
-        auto p_test = [&](int j, int t) { return mbar_test_wait(bar(C::B_PFULL + 2 * j + (t & 1)), (t >> 1) & 1); };
-        auto p_wait = [&](int j, int t, bool seen) -> bool {
-            if (__all_sync(0xffffffffu, seen)) return true;
-            return __all_sync(0xffffffffu, mbar_wait(bar(C::B_PFULL + 2 * j + (t & 1)), (t >> 1) & 1, wc, SITE_MMA_P));
-        };
-        // widths of tiles t, t+1, t+2 (w_cur, w_1, w_2)
-        KeyTiles<NK> tiles(runs);
-        int start, w_cur = 0, w_1 = 0, w_2 = 0;
-        bool ok = n_tiles > 0;
-        if (ok) {
-            tiles.next(start, w_cur);
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_QFULL), 0, wc, SITE_MMA_Q));
+            more = si.next(p, runs_tab, start, width, first, last);
         }
-        if (ok) ok = stage_wait(0, false);
-        if (ok) {
-            tc_fence_after();
-            for (int j = 0; j < nq; ++j) issue_s(j, 0, 0, w_cur, no_probe);
-        }
-        if (ok && n_tiles > 1) {
-            tiles.next(start, w_1);
-            if ((ok = stage_wait(1, false))) {
-                tc_fence_after();
-                for (int j = 0; j < nq; ++j) issue_s(j, 1, 1, w_1, no_probe);
-            }
-        }
-        bool p_seen0 = false, p_seen1 = false;  // early answers: P_0(t), P_1(t) ready
-        bool st_seen = n_tiles > 2 && ok && stage_test(2);  // early answer: tile t+2's stage landed
-        // Loop state of key tile t: width of tile t+2 (w_2), read in the previous iteration so
-        // that the next group's bookkeeping runs while MMAs of the current group are queued.
-        bool ahead = n_tiles > 2;
-        if (ahead) tiles.next(start, w_2);
-        for (int t = 0; t < n_tiles && ok; ++t) {
-            const int st = t % C::NS;
-            const int buf = t & 1;
-            const bool last = t + 1 == n_tiles;
-            const bool pv_commit = last || !use_bound;
-            bool st_next = false;
-            bool ahead_next = false;
-            int w_3 = 0;
-            // the work of the next key tile's loop head, done between MMAs of the last group
-            auto advance = [&] {
-                p_seen0 = t + 1 < n_tiles && p_test(0, t + 1);
-                st_next = t + 3 < n_tiles && stage_test(t + 3);
-                ahead_next = t + 3 < n_tiles;
-                if (ahead_next) tiles.next(start, w_3);
-            };
-            // query tile 0
-            if (!(ok = p_wait(0, t, p_seen0))) break;
-            tc_fence_after();
-            issue_pv(0, buf, st, w_cur, t == 0, pv_commit);
-            if (ahead) {
-                if (!(ok = stage_wait(t + 2, st_seen))) break;
-                tc_fence_after();
-            }
-            auto probe0 = [&] {
-                if (nq > 1)
-                    p_seen1 = p_test(1, t);
-                else
-                    advance();
-            };
-            if (ahead)
-                issue_s(0, buf, (t + 2) % C::NS, w_2, probe0);
-            else
-                probe0();
-            // query tile 1
-            if (nq > 1) {
-                if (!(ok = p_wait(1, t, p_seen1))) break;
-                tc_fence_after();
-                issue_pv(1, buf, st, w_cur, t == 0, pv_commit);
-                if (ahead)
-                    issue_s(1, buf, (t + 2) % C::NS, w_2, advance);
-                else
-                    advance();
-            }
-            st_seen = st_next;
-            ahead = ahead_next;
-            w_cur = w_1;
-            w_1 = w_2;
-            w_2 = w_3;
-            if (leader) tc_commit(bar(C::B_KVEMPTY + st));
-            __syncwarp();
-        }
-        // Every MMA this warp issued must complete before TMEM is released.
+        // Every tcgen05 instruction this warp issued must complete before TMEM is released.
         if (leader) tc_commit(bar(C::B_DRAIN));
         __syncwarp();
-        mbar_wait(bar(C::B_DRAIN), 0, wc, SITE_DRAIN, false);
+        wt.bar(p, bar(C::B_DRAIN), 0, SITE_DRAIN, false);
+        __syncwarp();
+    } else if (warp == kWarpPV) {
+        // ------------------------------------------------------------- tcgen05 issuer: PV
+        const bool leader = elect_one();
+        TileIter vi;
+        int n_items = 0;
+        long long n_pairs = 0;
+        // eligibility byte of the next item (prefetched one item ahead)
+        int nx_el = p.eligible && static_cast<int>(blockIdx.x) < p.total
+                        ? static_cast<int>(__ldg(p.eligible + static_cast<int>(blockIdx.x) / p.per_head))
+                        : 1;
+        bool online = true;
+        bool ok = true;
+        int start, width;
+        bool first, last;
+        bool more = vi.next(p, runs_tab, start, width, first, last);
+        bool p_seen = false, v_seen = false;  // readiness of tile g, tested ahead
+        for (int g = 0; ok && more; ++g) {
+            const int buf = g & (kNBuf - 1);
+            const bool t_first = first, t_last = last;
+            const int t_width = width;
+            if (first) {
+                online = !(p.mode == 0 && p.bound != nullptr && nx_el != 0);
+                const int nit = vi.it + static_cast<int>(gridDim.x);
+                nx_el = p.eligible && nit < p.total ? static_cast<int>(__ldg(p.eligible + nit / p.per_head)) : 1;
+                // the epilogue of the previous item must have read O
+                if (vi.local > 0 &&
+                    !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_OFREE), (vi.local - 1) & 1, SITE_MMA_OFREE))))
+                    break;
+            }
+            if (!__all_sync(0xffffffffu, v_seen) &&
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_VFULL + buf), (g >> 2) & 1, SITE_MMA_SLOT))))
+                break;
+            if (!__all_sync(0xffffffffu, p_seen) &&
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_PFULL + buf), (g >> 2) & 1, SITE_MMA_P))))
+                break;
+            tc_fence_after();
+            // O += P(g) V(g): A = P from the S buffer (16 keys = 8 columns per step)
+            const uint64_t b0 = smem_desc_sw128(vslot(buf), C::KV_PANEL, 1024);
+            if (leader)
+                mma_ts(tbase + C::T_O, tbase + C::t_s(buf), b0, C::IDESC_O, t_first ? 0u : 1u);
+            {
+                const int gn = g + 1, bn = gn & (kNBuf - 1);
+                p_seen = mbar_test_wait(bar(C::B_PFULL + bn), (gn >> 2) & 1);
+                v_seen = mbar_test_wait(bar(C::B_VFULL + bn), (gn >> 2) & 1);
+            }
+            if (leader) {
+#pragma unroll
+                for (int ks = 1; ks < kBufCols / 16; ++ks)
+                    if (ks < t_width / 16)
+                        mma_ts(tbase + C::T_O, tbase + C::t_s(buf) + ks * 16,
+                               b0 + static_cast<uint64_t>((ks * 16 * 128) >> 4), C::IDESC_O, 1u);
+                tc_commit(bar(C::B_BFREE + buf));
+                if (t_last)
+                    tc_commit(bar(C::B_OFULL));
+                else if (online)
+                    tc_commit(bar(C::B_PVDONE));
+            }
+            __syncwarp();
+            // coverage: the (query row, key) pairs this item's tiles consumed
+            n_pairs += static_cast<long long>(vi.valid) * t_width;
+            n_items += t_last ? 1 : 0;
+            more = vi.next(p, runs_tab, start, width, first, last);
+        }
+        if (p.stats && leader) {
+            if (n_items > 0) atomicAdd(&p.stats->items_done, n_items);
+            if (n_pairs > 0)
+                atomicAdd(reinterpret_cast<unsigned long long*>(&p.stats->pairs_visited),
+                          static_cast<unsigned long long>(n_pairs));
+        }
+        if (leader) tc_commit(bar(C::B_DRAIN + 1));
+        __syncwarp();
+        wt.bar(p, bar(C::B_DRAIN + 1), 0, SITE_DRAIN, false);
         __syncwarp();
     } else {
         // ------------------------------------------------------------- softmax + epilogue
-        const int j = warp >> 3;
-        if (j < nq) {
-            const int quarter = warp & 3;
-            const int hf = (warp >> 2) & 1;  // this warp's chunks: c = 2 i + hf
-            const int row = 32 * quarter + lane;
-            const int valid = j == 0 ? valid0 : valid1;
-            const bool rv = row < valid;
-            const int64_t grow = head_row0 + q_row0 + 128 * j + row;
-            const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
-            const uint32_t tO = tbase + lane_off + C::t_o(j) + hf * (D / 2);  // this warp's half of O
-            constexpr int OWN = (NK / 16 + 1) / 2;  // most chunks a warp owns
-            const float c2 = rv ? p.scale_log2 : 0.0f;
-            const float b_nat = (rv && p.bound) ? p.bound[grow] : 0.0f;
-            const float nb2 = use_bound ? -b_nat * kLog2e : 0.0f;
-            float m2 = -INFINITY;  // running max in log2 units (online path)
-            float l = 0.0f;        // sum of this warp's weights of the row
-            bool ok = true;
-            KeyTiles<NK> tiles(runs);
-            for (int t = 0; t < n_tiles; ++t) {
-                int start, width;
-                tiles.next(start, width);
-                const int nch = width / 16;  // 16-column chunks of this tile
-                const int buf = t & 1;
-                const uint32_t tS = tbase + lane_off + C::t_s(j, buf);
+        // Warp w: group w >> 2, lane quarter w & 3 (its 32 rows).  A thread owns one row of its
+        // group's tiles, all of the tile's keys; in the epilogue each group takes a share of O's
+        // columns.
+        const int group = warp >> 2;
+        const int quarter = warp & 3;
+        const int row = 32 * quarter + lane;
+        const uint32_t lane_off = static_cast<uint32_t>(32 * quarter) << 16;
+
+        // bound of this row and eligibility of the head of an item (prefetched one item ahead,
+        // so the loads are in flight while the previous item runs)
+        auto fetch = [&](int item, float& b, int& el) {
+            b = 0.0f;
+            el = 1;
+            if (item >= p.total) return;
+            const int h = item / p.per_head;
+            const int loc = item - h * p.per_head;
+            const int f = loc / p.n_qt;
+            const int qt = loc - f * p.n_qt;
+            if (p.bound && row < min(128, p.T - qt * 128))
+                b = __ldg(p.bound + static_cast<int64_t>(h) * p.N + f * p.T + qt * 128 + row);
+            if (p.eligible) el = __ldg(p.eligible + h);
+        };
+        float nx_b;
+        int nx_el;
+        fetch(blockIdx.x, nx_b, nx_el);
+
+        // current item: this row (h N + token), valid rows | bound flag << 8, bound, running state
+        int grow = 0, flags = 0;
+        float b_nat = 0.0f, m2 = -INFINITY, l = 0.0f;
+        // the previous item, whose epilogue waits until the tile walk reaches the next item:
+        // valid rows | bound flag << 8 | item << 9, or -1 for none
+        int pv_grow = 0, pv_flags = -1;
+        float pv_b = 0.0f, pv_m2 = 0.0f, pv_l = 0.0f;
+        uint32_t n_pv = 0;   // PVDONE phases waited for
+        bool ok = true;
+
+        // out = O / l for the rows of the previous item and this group's share of the columns
+        // (16-column chunks [cb, ce)); lse (and the row max) by group 0.  The row sum is split
+        // over the groups (each summed its own tiles); they exchange the parts first, and add
+        // them in group order.  False on abort.
+        auto epilogue = [&]() -> bool {
+            constexpr int NCH = D / 16;
+            const int cb = group * NCH / kGroups, ce = (group + 1) * NCH / kGroups;
+            const int item = pv_flags >> 9;
+            const uint32_t ls_count = sbase + C::MISC_OFF + 8u + 4u * quarter;
+            const uint32_t ls = sbase + C::LSUM_OFF + (item & 1) * (kGroups * 128 * 4) + 4u * row;
+            st_shared_f32(ls + group * 512, pv_l);
+            __syncwarp();
+            if (lane == 0) red_release_shared_add(ls_count, 1u);
+            if (!__all_sync(0xffffffffu,
+                            wt.counter(p, ls_count, kGroups * static_cast<uint32_t>(item + 1), SITE_SOFT_X)))
+                return false;
+            float l_row = ld_shared_f32(ls);
+#pragma unroll
+            for (int j = 1; j < kGroups; ++j) l_row += ld_shared_f32(ls + 512 * j);
+            const float inv_l = 1.0f / l_row;
+            const bool rvalid = row < (pv_flags & 0xff);
+            const bool ub = (pv_flags >> 8) & 1;
+            if (!__all_sync(0xffffffffu, wt.bar(p, bar(C::B_OFULL), item & 1, SITE_SOFT_O))) return false;
+            tc_fence_after();
+            const uint32_t tO = tbase + lane_off + C::T_O;
+            float4* dst = reinterpret_cast<float4*>(p.out + static_cast<int64_t>(pv_grow) * D);
+#pragma unroll
+            for (int j = 0; j < (NCH + kGroups - 1) / kGroups; ++j) {
+                const int c = cb + j;
+                if (c < ce) {
+                    float o[16];
+                    tmem_ld_x16(tO + 16 * c, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) reg_fence(o[i]);
+                    if (rvalid) {
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            dst[4 * c + e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
+                                                         o[4 * e + 3] * inv_l);
+                    }
+                }
+            }
+            // every read of O by this warp is complete: the next item may overwrite O
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(C::B_OFREE));
+            if (group == 0) {
+                const float m_nat = pv_m2 * kLn2;
+                bool under = false;
+                if (rvalid) {
+                    p.lse[pv_grow] = (ub ? pv_b : m_nat) + logf(l_row);
+                    if (p.rowmax) p.rowmax[pv_grow] = ub ? __int_as_float(0x7fc00000) : m_nat;
+                    under = ub ? !(l_row >= kFltMin) : (p.bound != nullptr && pv_b - m_nat >= kUnderflowGap);
+                }
+                const unsigned ubits = __ballot_sync(0xffffffffu, under);
+                if (p.stats && lane == 0 && ubits)
+                    atomicAdd(reinterpret_cast<unsigned long long*>(&p.stats->underflow_rows),
+                              static_cast<unsigned long long>(__popc(ubits)));
+            }
+            return true;
+        };
+
+        // Walk the items; per item, this group's tiles: every third tile on norm-bound items
+        // (tile t of an item goes to group t % 3), all tiles for group 0 on running-max items.
+        int g0 = 0;  // CTA tile index of the item's first tile
+        for (int item = blockIdx.x, local = 0; ok && item < p.total; item += gridDim.x, ++local) {
+            const int h = item / p.per_head;
+            const int loc = item - h * p.per_head;
+            const int f = loc / p.n_qt;
+            const int qt = loc - f * p.n_qt;
+            // the frame's key runs, cut into tiles of NK keys: n0 tiles of run 0 (the last of
+            // them w0 keys), then n1 of run 1 (the last w1 keys)
+            const int32_t* R = runs_tab + f * kRunStride;
+            const int l0 = R[2], l1 = R[0] > 1 ? R[4] : 0;
+            const int n0 = (l0 + p.NK - 1) / p.NK, n1 = (l1 + p.NK - 1) / p.NK;
+            const int w0 = l0 - (n0 - 1) * p.NK, w1 = l1 - (n1 - 1) * p.NK;
+            const int n = n0 + n1;
+            const bool use_bound = p.mode == 0 && p.bound != nullptr && nx_el != 0;
+            const int valid = min(128, p.T - qt * 128);
+            flags = valid | (use_bound ? 1 << 8 : 0);
+            grow = h * p.N + f * p.T + qt * 128 + row;
+            b_nat = nx_b;
+            fetch(item + static_cast<int>(gridDim.x), nx_b, nx_el);
+            m2 = -INFINITY;
+            l = 0.0f;
+            if (p.stats && p.mode == 0 && !use_bound && warp == 0 && lane == 0 && loc == 0)
+                atomicAdd(&p.stats->fallback_heads, 1);
+            const int step = use_bound ? kGroups : 1;
+            // tile t of the item goes to group t % 3: the split of the row sum over the groups, and
+            // so its rounding, depends on the item alone, not on what the CTA ran before it
+            int t = use_bound ? group : (group == 0 ? 0 : n);
+            // a group that does not take the item's first tile finishes the previous item now;
+            // the one that does, right after producing that tile's P
+            if (t != 0 && pv_flags >= 0) {
+                if (!(ok = epilogue())) break;
+                pv_flags = -1;
+            }
+            for (; t < n; t += step) {
+                const int g = g0 + t;
+                const int width = t == n0 - 1 ? w0 : (t == n - 1 ? w1 : p.NK);
+                const int nch = width / 16;
+                const int buf = g & (kNBuf - 1);
+                const uint32_t tS = tbase + lane_off + C::t_s(buf);
+                const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
                 // the vote keeps the warp converged for the warp-collective TMEM accesses
-                if (!(ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_SFULL + 2 * j + buf), (t >> 1) & 1, wc,
-                                                             SITE_SOFT_S))))
+                if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
                     break;
                 tc_fence_after();
-                float s[16 * OWN];  // own chunks, compact
-                uint32_t pk[8 * OWN];
-#pragma unroll
-                for (int i = 0; i < OWN; ++i)
-                    if (2 * i + hf < nch) tmem_ld_x16(tS + 16 * (2 * i + hf), s + 16 * i);
-                tmem_ld_wait();
-#pragma unroll
-                for (int i = 0; i < 16 * OWN; ++i) reg_fence(s[i]);
-                // Two packed partial sums of the fp32 weights (short add chains).
-                float2 acc[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-                float alpha = 1.0f, m_new = m2;
-                float2 off = make_float2(nb2, nb2);
+                // The tile is read in halves of up to 32 keys (chunks 2hh, 2hh + 1), one loop body
+                // for both, so the hot code stays small.
+                float alpha = 1.0f, m_new = m2, nb2 = -b_nat * kLog2e;
                 if (!use_bound) {
-                    // The running max over the whole row.  The two warps of the row exchange
-                    // the maxima of their own chunks through shared memory: reading the other
-                    // warp's chunks from TMEM could race with its P being written over them.
-                    float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    // running max: a first pass over the tile for its row max (a thread owns the
+                    // whole row, so no exchange), then the exponentials as on norm-bound tiles
+                    float mx = -INFINITY;
+#pragma unroll 1
+                    for (int hh = 0; hh < 2; ++hh) {
+                        if (2 * hh >= nch) break;
+                        float s[32];
+                        tmem_ld_x16(tS + 32 * hh, s);
+                        if (2 * hh + 1 < nch) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < OWN; ++i) {
-                        if (2 * i + hf < nch) {
+                        for (int i = 0; i < 32; ++i) reg_fence(s[i]);
+                        float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) mx[e & 3] = fmaxf(mx[e & 3], s[16 * i + e]);
+                        for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
+                        if (2 * hh + 1 < nch) {
+#pragma unroll
+                            for (int e = 16; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
                         }
+                        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
                     }
-                    const float mine = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-                    // slots double-buffered by key-tile parity: a warp writes tile t+2's slot only
-                    // after its partner has written tile t+1's, i.e. after it read tile t's
-                    float* mslot = reinterpret_cast<float*>(sgen + C::MMAX_OFF) + (((t & 1) * 2 + j) * 2) * 128;
-                    mslot[hf * 128 + row] = mine;
-                    __syncwarp();
-                    const uint32_t xa = sbase + C::MISC_OFF + 24u + 4u * static_cast<uint32_t>(4 * j + quarter);
-                    if (lane == 0) red_release_shared_add(xa, 1u);
-                    if (!(ok = __all_sync(0xffffffffu,
-                                          counter_wait(xa, 2u * static_cast<uint32_t>(t + 1), wc, SITE_SOFT_S))))
-                        break;
-                    const float theirs = mslot[(1 - hf) * 128 + row];
-                    m_new = fmaxf(m2, fmaxf(mine, theirs) * c2);
+                    m_new = fmaxf(m2, mx * c2);
                     alpha = ex2(m2 - m_new);
-                    off = make_float2(-m_new, -m_new);
+                    nb2 = -m_new;
                 }
-                const float2 cc = make_float2(c2, c2);
+                // p = 2^(s c2 + nb2), packed to bf16 over the S columns just read; four partial
+                // sums of the fp32 weights (short add chains)
+                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll 1
+                for (int hh = 0; hh < 2; ++hh) {
+                    if (2 * hh >= nch) break;
+                    const bool two = 2 * hh + 1 < nch;
+                    float s[32];
+                    uint32_t pk[16];
+                    tmem_ld_x16(tS + 32 * hh, s);
+                    if (two) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
+                    tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < OWN; ++i) {
-                    if (2 * i + hf < nch) {
+                    for (int i = 0; i < 32; ++i) reg_fence(s[i]);
 #pragma unroll
-                        for (int e = 8 * i; e < 8 * i + 8; ++e) {
-                            const float2 x = ffma2(make_float2(s[2 * e], s[2 * e + 1]), cc, off);
-                            const float p0 = ex2(x.x);
-                            const float p1 = ex2(x.y);
-                            pk[e] = pack_bf16x2(p0, p1);
-                            acc[e & 1] = fadd2(acc[e & 1], make_float2(p0, p1));
+                    for (int i = 0; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                    for (int i = 0; i < 16; i += 4) {
+                        a0 += s[i];
+                        a1 += s[i + 1];
+                        a2 += s[i + 2];
+                        a3 += s[i + 3];
+                    }
+                    tmem_st_x8(tS + 32 * hh, pk);
+                    if (two) {
+#pragma unroll
+                        for (int i = 16; i < 32; i += 4) {
+                            a0 += s[i];
+                            a1 += s[i + 1];
+                            a2 += s[i + 2];
+                            a3 += s[i + 3];
                         }
+                        tmem_st_x8(tS + 32 * hh + 16, pk + 8);
                     }
                 }
-                l = l * alpha + ((acc[0].x + acc[0].y) + (acc[1].x + acc[1].y));
-                if (!use_bound && t > 0) {
-                    // O_j may be rescaled only once PV_j(t-1) is done (committed every tile here)
-                    if (!(ok = __all_sync(0xffffffffu,
-                                          mbar_wait(bar(C::B_PVDONE + j), (t - 1) & 1, wc, SITE_SOFT_O))))
-                        break;
+                l = l * alpha + ((a0 + a1) + (a2 + a3));
+                if (!use_bound && t != 0) {
+                    // O may be rescaled only once PV of the item's previous tile is done
+                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_PVDONE), n_pv & 1, SITE_SOFT_O)))) break;
+                    ++n_pv;
                     tc_fence_after();
                     if (__any_sync(0xffffffffu, m_new > m2)) {
-                        // running max moved: rescale this warp's half of the accumulator before
-                        // PV_j(t) may start
+                        // running max moved: rescale the row's accumulator
+                        const uint32_t tO = tbase + lane_off + C::T_O;
 #pragma unroll 1
-                        for (int c = 0; c < D / 32; ++c) {
+                        for (int c = 0; c < D / 16; ++c) {
                             float o[16];
-                            tmem_load_cols<16>(tO + 16 * c, o);
+                            tmem_ld_x16(tO + 16 * c, o);
+                            tmem_ld_wait();
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) o[e] *= alpha;
+                            for (int e = 0; e < 16; ++e) {
+                                reg_fence(o[e]);
+                                o[e] *= alpha;
+                            }
                             tmem_st_x16(tO + 16 * c, o);
                         }
                     }
                 }
                 m2 = m_new;
-#pragma unroll
-                for (int i = 0; i < OWN; ++i)
-                    if (2 * i + hf < nch) tmem_st_x8(tS + 16 * (2 * i + hf), pk + 8 * i);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::B_PFULL + 2 * j + buf));
-            }
-            // the last PV: phase n_tiles - 1 on running-max heads (every PV committed), the
-            // only phase 0 on norm-bound heads
-            if (ok && n_tiles > 0)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(C::B_PVDONE + j), use_bound ? 0 : (n_tiles - 1) & 1, wc,
-                                                       SITE_SOFT_O));
-            // The row sum is split over the two warps of the row: exchange the halves.
-            float* lsum = reinterpret_cast<float*>(sgen + C::LSUM_OFF) + (2 * j) * 128;
-            lsum[hf * 128 + row] = l;
-            __syncwarp();
-            if (lane == 0) red_release_shared_add(xcount_addr(j), 1u);
-            if (ok) ok = __all_sync(0xffffffffu, counter_wait(xcount_addr(j), 8u, wc, SITE_SOFT_O));
-            if (ok) {
-                tc_fence_after();
-                const float l_row = l + lsum[(1 - hf) * 128 + row];
-                const float inv_l = 1.0f / l_row;
-                float* orow = p.out + grow * D + hf * (D / 2);
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    float o[16];
-                    tmem_load_cols<16>(tO + 16 * c, o);
-                    if (rv) {
-                        float4* dst = reinterpret_cast<float4*>(orow + 16 * c);
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            dst[e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
-                                                 o[4 * e + 3] * inv_l);
-                    }
-                }
-                if (hf == 0) {
-                    const float m_nat = m2 * kLn2;
-                    bool under = false;
-                    if (rv) {
-                        p.lse[grow] = (use_bound ? b_nat : m_nat) + logf(l_row);
-                        if (p.rowmax) p.rowmax[grow] = use_bound ? __int_as_float(0x7fc00000) : m_nat;
-                        under = use_bound ? !(l_row >= kFltMin)
-                                          : (p.bound != nullptr && b_nat - m_nat >= kUnderflowGap);
-                    }
-                    const unsigned ub = __ballot_sync(0xffffffffu, under);
-                    if (p.stats && lane == 0 && ub)
-                        atomicAdd(reinterpret_cast<unsigned long long*>(&p.stats->underflow_rows),
-                                  static_cast<unsigned long long>(__popc(ub)));
+                if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
+                if (pv_flags >= 0) {
+                    if (!(ok = epilogue())) break;
+                    pv_flags = -1;
                 }
             }
+            if (!ok) break;
+            pv_flags = flags | (local << 9);
+            pv_b = b_nat;
+            pv_m2 = m2;
+            pv_l = l;
+            pv_grow = grow;
+            g0 += n;
         }
+        if (ok && pv_flags >= 0) ok = epilogue();
     }
 
     // ------------------------------------------------------------- teardown
     tc_fence_before();
     __syncthreads();
-    if (warp == kWarpMma) {
+    if (warp == kWarpS) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tbase, C::TMEM_COLS);
@@ -598,48 +781,46 @@ __global__ void fsa_selftest_wait_kernel(long long limit, int* status)
     }
 }
 
-template <int D, int NK>
+template <int D>
 static int launch_attn(const AttnLaunch& L)
 {
-    using C = AttnCfg<D, NK>;
-    auto kern = fsa_attn_fwd_kernel<D, NK>;
+    using C = AttnCfg<D>;
+    auto kern = fsa_attn_fwd_kernel<D>;
     static bool attr_done = false;  // per instantiation
     if (!attr_done) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-            cudaSuccess)
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (e != cudaSuccess) {
+            note_cuda_error(e);
             return -3;
+        }
         attr_done = true;
     }
-    const dim3 grid(static_cast<unsigned>(L.params.n_items) * static_cast<unsigned>(L.H));
+    if (L.params.total <= 0) return 0;
+    const unsigned grid = static_cast<unsigned>(L.params.total < L.sms ? L.params.total : L.sms);
     kern<<<grid, kAttnThreads, C::SMEM_BYTES, L.stream>>>(*L.tmQ, *L.tmK, *L.tmV, L.params);
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return launch_status();
 }
 
-#define FSA_FOR_EACH_TILE(X) \
-    X(64, 16) X(64, 32) X(64, 48) X(64, 64) X(128, 16) X(128, 32) X(128, 48) X(128, 64)
-
-int attn_smem_bytes(int D, int NK)
+int attn_smem_bytes(int D)
 {
-#define FSA_SMEM_CASE(d, nk) \
-    if (D == d && NK == nk) return AttnCfg<d, nk>::SMEM_BYTES;
-    FSA_FOR_EACH_TILE(FSA_SMEM_CASE)
-#undef FSA_SMEM_CASE
+    if (D == 64) return AttnCfg<64>::SMEM_BYTES;
+    if (D == 128) return AttnCfg<128>::SMEM_BYTES;
     return -1;
 }
 
 int launch_attention(const AttnLaunch& L)
 {
-#define FSA_ATTN_CASE(d, nk) \
-    if (L.D == d && L.NK == nk) return launch_attn<d, nk>(L);
-    FSA_FOR_EACH_TILE(FSA_ATTN_CASE)
-#undef FSA_ATTN_CASE
+    static_assert(kMaxKeyTile == kBufCols, "one key tile fills an S buffer at most");
+    if (L.params.NK < 16 || L.params.NK > kMaxKeyTile || L.params.NK % 16 != 0) return -2;
+    if (L.D == 64) return launch_attn<64>(L);
+    if (L.D == 128) return launch_attn<128>(L);
     return -2;
 }
 
 int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream)
 {
     fsa_selftest_wait_kernel<<<1, 32, 0, stream>>>(limit, d_status);
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return launch_status();
 }
 
 }  // namespace fsa

@@ -9,21 +9,22 @@
 
 namespace fsa {
 
-// Key runs of one query frame: [n_runs, start_0, len_0, start_1, len_1, ...] in tokens of a
-// head; every run is a union of whole frames, ascending, disjoint.
-constexpr int kMaxRuns = 4;
-
-// Largest key tile the attention kernel supports (for D = 64 and 128): each of the two query
-// tiles holds two S buffers (NK columns each, P written over S) and O (D columns) in 256 TMEM
-// columns, and a softmax thread keeps its half of a tile row in registers.
-constexpr int kMaxKeyTile(int D) { return 64; }
+// Key runs of one query frame: [n_runs, start_0, len_0, start_1, len_1] in tokens of a head;
+// every run is a union of whole frames, ascending, disjoint.  A frame's key set is a window
+// of consecutive frames plus the reference frame, so it never takes more than two runs.
+constexpr int kMaxRuns = 2;
 constexpr int kRunStride = 1 + 2 * kMaxRuns;
 
+// Largest key tile of the attention kernel (its four S buffers hold 64 columns each).
+constexpr int kMaxKeyTile = 64;
+
 struct AttnParams {
-    const int32_t* items;  // [n_items][4]: query frame, first query row (token), valid rows tile 0, tile 1
     const int32_t* runs;   // [F][kRunStride]
-    int n_items;
-    int N;                 // tokens per head
+    int F, T, N;           // frames, tokens per frame, tokens per head
+    int n_qt;              // 128-row query tiles per frame, ceil(T / 128)
+    int per_head;          // work items per head, F * n_qt
+    int total;             // work items, H * per_head
+    int NK;                // keys per tile (multiple of 16, at most kMaxKeyTile)
     float scale_log2;      // c * log2(e)
     int mode;              // 0 norm_bound, 1 online_max
     const float* bound;    // [H][N] or null
@@ -36,16 +37,22 @@ struct AttnParams {
 };
 
 struct AttnLaunch {
-    int D, NK, H;
-    const CUtensorMap* tmQ;
-    const CUtensorMap* tmK;
+    int D, H;
+    int sms;               // persistent grid: min(sms, work items) CTAs
+    const CUtensorMap* tmQ;  // boxes of 128 rows
+    const CUtensorMap* tmK;  // boxes of NK rows
     const CUtensorMap* tmV;
     AttnParams params;
     cudaStream_t stream;
 };
 
+// Records the code of a failed CUDA call for fsa_last_cuda_error (per host thread).
+void note_cuda_error(int code);
+// cudaGetLastError after a launch: 0 on success, else -3 with the code recorded.
+int launch_status();
+
 int launch_attention(const AttnLaunch& L);
-int attn_smem_bytes(int D, int NK);
+int attn_smem_bytes(int D);
 int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);
 
 struct NormsLaunch {

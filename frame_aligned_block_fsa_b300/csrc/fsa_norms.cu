@@ -410,13 +410,13 @@ static int launch_norms_d(const NormsLaunch& L)
         query_bounds_kernel<D, false><<<grid, kNormThreads, 0, L.stream>>>(
             L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum, nullptr, L.qnorm, L.bound, L.gmax, rows_per_block);
     eligibility_kernel<<<(L.H + 127) / 128, 128, 0, L.stream>>>(L.gmax, L.tau, L.eligible, L.H);
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return launch_status();
 }
 
 int launch_eligibility(const unsigned* gmax, float tau, uint8_t* eligible, int H, cudaStream_t stream)
 {
     eligibility_kernel<<<(H + 127) / 128, 128, 0, stream>>>(gmax, tau, eligible, H);
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return launch_status();
 }
 
 int launch_norms(const NormsLaunch& L)

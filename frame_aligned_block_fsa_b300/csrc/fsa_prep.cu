@@ -616,7 +616,7 @@ static int launch_prep_d(const PrepLaunch& L)
     if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fsa_prep_kernel<D>), dim3(grid), dim3(kPrepThreads),
                                     args, PrepCfg::SMEM_BYTES, L.stream) != cudaSuccess)
         return -3;
-    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+    return launch_status();
 }
 
 int launch_prep(const PrepLaunch& L)

@@ -13,6 +13,12 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Generic pointer to a shared-memory address.
+__device__ __forceinline__ void* smem_generic(uint32_t addr)
+{
+    return __cvta_shared_to_generic(addr);
+}
+
 // One lane of a converged warp: true in exactly one lane (the same lane on every call
 // while the whole warp is active).
 __device__ __forceinline__ bool elect_one()
@@ -48,15 +54,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+// Potentially blocking test: the thread is suspended (it issues nothing) until the phase
+// completes or about `suspend_ns` nanoseconds have passed.  A waiting warp therefore leaves the
+// issue slots of its SM sub-partition to the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t suspend_ns = 20000u)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
@@ -119,15 +128,20 @@ __device__ __forceinline__ void red_release_shared_add(uint32_t addr, uint32_t v
 }
 
 // Wait until the counter reaches `target` (bounded like mbar_wait).  The abort flag and the
-// clock are checked once per 32 polls, so a poll is one shared load and a compare.
+// clock are checked once per 8 polls; after the first polls the waiter sleeps between polls,
+// so a long wait leaves the sub-partition's issue slots to the warps that do the work.
 __device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, const WaitCtl& w, int site)
 {
     if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
     const long long t0 = clock64();
+    uint32_t nap = 0;
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
+        for (int i = 0; i < 8; ++i) {
             if (static_cast<int>(ld_acquire_shared(addr) - target) >= 0) return true;
+            if (nap) __nanosleep(nap);
+        }
+        nap = nap ? min(nap * 2u, 256u) : 16u;
         if (*w.abort) return false;
         if (clock64() - t0 > w.limit) {
             *w.abort = 1;
@@ -136,6 +150,19 @@ __device__ __forceinline__ bool counter_wait(uint32_t addr, uint32_t target, con
             return false;
         }
     }
+}
+
+// Plain shared-memory accesses by 32-bit address (no 64-bit generic pointer held).
+__device__ __forceinline__ void st_shared_f32(uint32_t addr, float v)
+{
+    asm volatile("st.shared::cta.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ float ld_shared_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared::cta.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
 }
 
 // ----------------------------------------------------------------------------- TMA
@@ -268,6 +295,15 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
+// Copy a 128-row x 256-bit (16 bf16 per row) matrix from shared memory, described by a matrix
+// descriptor like an MMA operand, into 8 consecutive TMEM columns of lanes 0-127: row r lands in
+// lane r, its bf16 pairs in consecutive columns, the layout of an MMA A operand in TMEM.
+// Asynchronous; ordered before the MMAs the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // 32 lanes x 32-bit, 16 consecutive columns per thread (thread t <- lane base+t).  No wait.
 __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float* v)
 {
@@ -280,6 +316,16 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, float* v)
           "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
+}
+
+// 32 lanes x 32-bit, 8 consecutive columns per thread.  No wait.
+__device__ __forceinline__ void tmem_ld_x8(uint32_t taddr, float* v)
+{
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld_wait()

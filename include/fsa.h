@@ -63,10 +63,12 @@ typedef struct fsa_stats {
     int32_t error;          /* 0, or FSA_ERR_TIMEOUT if a bounded wait inside a kernel gave up */
     int32_t timeout_site;   /* diagnostic: which wait gave up (0 if none) */
     int32_t fallback_heads; /* heads run with the running max although norm_bound was requested */
-    int32_t reserved0;
+    int32_t items_done;     /* attention work items (128-row query tiles of one head) completed */
     int64_t underflow_rows; /* rows whose bound gap is >= 126 ln 2 (known only where the row max is
                                tracked and a bound is available) or whose row sum underflowed */
-    int64_t reserved1;
+    int64_t pairs_visited;  /* coverage: sum over completed work items of (valid query rows) x
+                               (keys the item's tiles consumed); a complete call visits every
+                               active block pair once, H * nnz * block^2 */
 } fsa_stats_t;
 
 /*
@@ -107,13 +109,14 @@ int fsa_plan_export(fsa_plan_t plan, int32_t* row_ptr, int32_t* col_idx, int64_t
 int fsa_plan_set_tau(fsa_plan_t plan, float tau);
 
 /*
- * fsa_plan_set_key_tile -- keys per tensor-core tile: 0 = automatic (the kernel's largest,
- * 64), else a multiple of 16 in [16, 128].  Every key run (a
- * whole number of frames) is cut into tiles of this many keys and one last narrower tile
- * of the rest (a multiple of 16, since T is); no tile is partially masked.  A tile above
- * the limit for the call's D makes fsa_forward* return FSA_ERR_UNSUPPORTED.  Results are
- * bitwise independent of `block`; they may change in the last bits with the key tile
- * (summation order).
+ * fsa_plan_set_key_tile -- keys per tensor-core tile: 0 = automatic (64, the kernel's
+ * largest), else a multiple of 16 in [16, 128].  Every key run (a whole number of frames) is
+ * cut into tiles of this many keys and one last narrower tile of the rest (a multiple of 16,
+ * since T is); no tile is partially masked.  Results are bitwise independent of `block`;
+ * they may change in the last bits with the key tile (summation order).
+ * Errors: FSA_ERR_INVALID_ARG for a NULL plan or a key tile outside that set; a tile above
+ * the attention kernel's limit (64 keys, the width of its S buffers in TMEM) makes
+ * fsa_forward* return FSA_ERR_UNSUPPORTED before any device work.
  */
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
 
@@ -260,6 +263,13 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
  */
 int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, int D, fsa_plan_t plan,
                       float* qnorm, float* kmax, float* bound, uint8_t* eligible, void* stream);
+
+/*
+ * fsa_last_cuda_error -- the code of the last CUDA call that failed inside this library on the
+ * calling host thread (a cudaError_t value; driver CUresult values are returned plus 100000),
+ * or 0; reading it clears it.  Diagnostic companion of FSA_ERR_CUDA.  Host only.
+ */
+int fsa_last_cuda_error(void);
 
 /* Human-readable name of a status code (static storage). */
 const char* fsa_status_string(int status);
