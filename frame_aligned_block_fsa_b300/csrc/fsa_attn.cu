@@ -93,22 +93,27 @@ struct AttnCfg {
     static constexpr int B_QFULL = 2 * kNBuf;          // the staged Q tile landed
     static constexpr int B_QEMPTY = B_QFULL + 1;       // its copy into TMEM is done
     static constexpr int B_SFULL = B_QEMPTY + 1;       // kNBuf: S in buffer b complete (K slot b free)
-    static constexpr int B_PFULL = B_SFULL + kNBuf;    // kNBuf: P in buffer b written (one group's warps)
-    static constexpr int B_PVDONE = B_PFULL + kNBuf;   // PV of a running-max tile done (not the item's last)
-    static constexpr int B_OFULL = B_PVDONE + 1;       // the last PV of an item done: O final
+    // kNBuf: P in buffer b written: kSoftWarps arrivals, 3 from each warp of the owning group
+    // on norm-bound tiles, 1 from every softmax warp on running-max tiles
+    static constexpr int B_PFULL = B_SFULL + kNBuf;
+    static constexpr int B_OFULL = B_PFULL + kNBuf;    // the last PV of an item done: O final
     static constexpr int B_OFREE = B_OFULL + 1;        // the epilogue has read O (all softmax warps)
     static constexpr int B_BFREE = B_OFREE + 1;        // kNBuf: PV of buffer b's tile done (S buffer b and V
                                                        // slot b free)
     static constexpr int B_QDONE = B_BFREE + kNBuf;    // 2: the last S MMA of an item using Q slot s done
     static constexpr int B_DRAIN = B_QDONE + 2;        // 2: everything an issuer issued is done
     static constexpr int N_BARS = B_DRAIN + 2;
-    // abort flag (+0), TMEM address (+4), per lane quarter: row-sum exchange counters (+8 .. +24)
+    // abort flag (+0), TMEM address (+4), per lane quarter: row-sum exchange counters (+8 .. +24),
+    // tile-max exchange counters (+24 .. +40)
     static constexpr int MISC_OFF = BAR_OFF + 8 * N_BARS;
-    static constexpr int MISC_BYTES = 32;
+    static constexpr int MISC_BYTES = 48;
     // per item parity, group, row: a group's part of the row sum (epilogue)
     static constexpr int LSUM_OFF = (MISC_OFF + MISC_BYTES + 15) & ~15;
     static constexpr int LSUM_BYTES = 2 * kGroups * 128 * 4;
-    static constexpr int RUNS_OFF = LSUM_OFF + LSUM_BYTES;
+    // per exchange parity, group, row: a group's tile max (running-max tiles)
+    static constexpr int MMAX_OFF = LSUM_OFF + LSUM_BYTES;
+    static constexpr int MMAX_BYTES = 2 * kGroups * 128 * 4;
+    static constexpr int RUNS_OFF = MMAX_OFF + MMAX_BYTES;
     static constexpr int SMEM_USED = RUNS_OFF + kSmemRunFrames * kRunStride * 4;
     // room to align the buffers to 1024 B, and at least half of the SM's shared memory, so two
     // CTAs never share an SM (each takes all 512 TMEM columns)
@@ -277,9 +282,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(bar(C::B_QEMPTY), 1);
         for (int b = 0; b < kNBuf; ++b) {
             mbar_init(bar(C::B_SFULL + b), 1);
-            mbar_init(bar(C::B_PFULL + b), kGroupWarps);
+            mbar_init(bar(C::B_PFULL + b), kSoftWarps);
         }
-        mbar_init(bar(C::B_PVDONE), 1);
         mbar_init(bar(C::B_OFULL), 1);
         mbar_init(bar(C::B_OFREE), kSoftWarps);
         for (int b = 0; b < kNBuf; ++b) mbar_init(bar(C::B_BFREE + b), 1);
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(bar(C::B_QDONE + i), 1);
             mbar_init(bar(C::B_DRAIN + i), 1);
         }
-        for (int i = 0; i < 4; ++i) counters[i] = 0;
+        for (int i = 0; i < 8; ++i) counters[i] = 0;
         *reinterpret_cast<volatile int*>(sgen + C::MISC_OFF) = 0;  // abort flag
         fence_mbar_init();
     }
@@ -427,11 +431,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         TileIter vi;
         int n_items = 0;
         long long n_pairs = 0;
-        // eligibility byte of the next item (prefetched one item ahead)
-        int nx_el = p.eligible && static_cast<int>(blockIdx.x) < p.total
-                        ? static_cast<int>(__ldg(p.eligible + static_cast<int>(blockIdx.x) / p.per_head))
-                        : 1;
-        bool online = true;
         bool ok = true;
         int start, width;
         bool first, last;
@@ -442,9 +441,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const bool t_first = first, t_last = last;
             const int t_width = width;
             if (first) {
-                online = !(p.mode == 0 && p.bound != nullptr && nx_el != 0);
-                const int nit = vi.it + static_cast<int>(gridDim.x);
-                nx_el = p.eligible && nit < p.total ? static_cast<int>(__ldg(p.eligible + nit / p.per_head)) : 1;
                 // the epilogue of the previous item must have read O
                 if (vi.local > 0 &&
                     !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_OFREE), (vi.local - 1) & 1, SITE_MMA_OFREE))))
@@ -473,10 +469,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         mma_ts(tbase + C::T_O, tbase + C::t_s(buf) + ks * 16,
                                b0 + static_cast<uint64_t>((ks * 16 * 128) >> 4), C::IDESC_O, 1u);
                 tc_commit(bar(C::B_BFREE + buf));
-                if (t_last)
-                    tc_commit(bar(C::B_OFULL));
-                else if (online)
-                    tc_commit(bar(C::B_PVDONE));
+                if (t_last) tc_commit(bar(C::B_OFULL));
             }
             __syncwarp();
             // coverage: the (query row, key) pairs this item's tiles consumed
@@ -523,13 +516,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         fetch(blockIdx.x, nx_b, nx_el);
 
         // current item: this row (h N + token), valid rows | bound flag << 8, bound, running state
+        // m2: the reference of the exponentials on running-max items, mt: the row max (both in
+        // log2 units of the logits)
         int grow = 0, flags = 0;
-        float b_nat = 0.0f, m2 = -INFINITY, l = 0.0f;
+        float b_nat = 0.0f, m2 = -INFINITY, mt = -INFINITY, l = 0.0f;
         // the previous item, whose epilogue waits until the tile walk reaches the next item:
         // valid rows | bound flag << 8 | item << 9, or -1 for none
         int pv_grow = 0, pv_flags = -1;
-        float pv_b = 0.0f, pv_m2 = 0.0f, pv_l = 0.0f;
-        uint32_t n_pv = 0;   // PVDONE phases waited for
+        float pv_b = 0.0f, pv_m2 = 0.0f, pv_mt = 0.0f, pv_l = 0.0f;
+        uint32_t n_mx = 0;   // tile-max exchanges done
         bool ok = true;
 
         // out = O / l for the rows of the previous item and this group's share of the columns
@@ -580,10 +575,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(C::B_OFREE));
             if (group == 0) {
-                const float m_nat = pv_m2 * kLn2;
+                const float m_nat = pv_mt * kLn2;
                 bool under = false;
                 if (rvalid) {
-                    p.lse[pv_grow] = (ub ? pv_b : m_nat) + logf(l_row);
+                    p.lse[pv_grow] = (ub ? pv_b : pv_m2 * kLn2) + logf(l_row);
                     if (p.rowmax) p.rowmax[pv_grow] = ub ? __int_as_float(0x7fc00000) : m_nat;
                     under = ub ? !(l_row >= kFltMin) : (p.bound != nullptr && pv_b - m_nat >= kUnderflowGap);
                 }
@@ -617,120 +612,185 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             b_nat = nx_b;
             fetch(item + static_cast<int>(gridDim.x), nx_b, nx_el);
             m2 = -INFINITY;
+            mt = -INFINITY;
             l = 0.0f;
             if (p.stats && p.mode == 0 && !use_bound && warp == 0 && lane == 0 && loc == 0)
                 atomicAdd(&p.stats->fallback_heads, 1);
-            const int step = use_bound ? kGroups : 1;
-            // tile t of the item goes to group t % 3: the split of the row sum over the groups, and
-            // so its rounding, depends on the item alone, not on what the CTA ran before it
-            int t = use_bound ? group : (group == 0 ? 0 : n);
-            // a group that does not take the item's first tile finishes the previous item now;
-            // the one that does, right after producing that tile's P
-            if (t != 0 && pv_flags >= 0) {
-                if (!(ok = epilogue())) break;
-                pv_flags = -1;
-            }
-            for (; t < n; t += step) {
-                const int g = g0 + t;
-                const int width = t == n0 - 1 ? w0 : (t == n - 1 ? w1 : p.NK);
-                const int nch = width / 16;
-                const int buf = g & (kNBuf - 1);
-                const uint32_t tS = tbase + lane_off + C::t_s(buf);
-                const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
-                // the vote keeps the warp converged for the warp-collective TMEM accesses
-                if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
-                    break;
-                tc_fence_after();
-                // The tile is read in halves of up to 32 keys (chunks 2hh, 2hh + 1), one loop body
-                // for both, so the hot code stays small.
-                float alpha = 1.0f, m_new = m2, nb2 = -b_nat * kLog2e;
-                if (!use_bound) {
-                    // running max: a first pass over the tile for its row max (a thread owns the
-                    // whole row, so no exchange), then the exponentials as on norm-bound tiles
-                    float mx = -INFINITY;
+            // Norm-bound items: tile t goes to group t % 3 (the split of the row sum over the groups,
+            // and so its rounding, depends on the item alone).  Running-max items: every group takes
+            // every tile, each its own 16-key chunks (chunk c to group c % 3).  One loop per kind,
+            // so each stays small.
+            if (use_bound) {
+                // a group that does not take the item's first tile finishes the previous item
+                // now; the one that does, right after producing that tile's P
+                if (group != 0 && pv_flags >= 0) {
+                    if (!(ok = epilogue())) break;
+                    pv_flags = -1;
+                }
+                for (int t = group; t < n; t += kGroups) {
+                    const int g = g0 + t;
+                    const int width = t == n0 - 1 ? w0 : (t == n - 1 ? w1 : p.NK);
+                    const int nch = width / 16;
+                    const int buf = g & (kNBuf - 1);
+                    const uint32_t tS = tbase + lane_off + C::t_s(buf);
+                    const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
+                    // the vote keeps the warp converged for the warp-collective TMEM accesses
+                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
+                        break;
+                    tc_fence_after();
+                    // p = 2^(s c2 - b log2 e) over the whole tile, read in halves of up to 32 keys
+                    // (chunks 2hh, 2hh + 1), one loop body for both, so the hot code stays small;
+                    // packed to bf16 over the S columns just read; four partial sums of the fp32
+                    // weights (short add chains)
+                    const float nb2 = -b_nat * kLog2e;
+                    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll 1
                     for (int hh = 0; hh < 2; ++hh) {
                         if (2 * hh >= nch) break;
+                        const bool two = 2 * hh + 1 < nch;
                         float s[32];
+                        uint32_t pk[16];
                         tmem_ld_x16(tS + 32 * hh, s);
-                        if (2 * hh + 1 < nch) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
+                        if (two) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) reg_fence(s[i]);
-                        float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-                        if (2 * hh + 1 < nch) {
+                        for (int i = 0; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
 #pragma unroll
-                            for (int e = 16; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-                        }
-                        mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-                    }
-                    m_new = fmaxf(m2, mx * c2);
-                    alpha = ex2(m2 - m_new);
-                    nb2 = -m_new;
-                }
-                // p = 2^(s c2 + nb2), packed to bf16 over the S columns just read; four partial
-                // sums of the fp32 weights (short add chains)
-                float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll 1
-                for (int hh = 0; hh < 2; ++hh) {
-                    if (2 * hh >= nch) break;
-                    const bool two = 2 * hh + 1 < nch;
-                    float s[32];
-                    uint32_t pk[16];
-                    tmem_ld_x16(tS + 32 * hh, s);
-                    if (two) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
-                    tmem_ld_wait();
+                        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) reg_fence(s[i]);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-                    for (int i = 0; i < 16; i += 4) {
-                        a0 += s[i];
-                        a1 += s[i + 1];
-                        a2 += s[i + 2];
-                        a3 += s[i + 3];
-                    }
-                    tmem_st_x8(tS + 32 * hh, pk);
-                    if (two) {
-#pragma unroll
-                        for (int i = 16; i < 32; i += 4) {
+                        for (int i = 0; i < 16; i += 4) {
                             a0 += s[i];
                             a1 += s[i + 1];
                             a2 += s[i + 2];
                             a3 += s[i + 3];
                         }
-                        tmem_st_x8(tS + 32 * hh + 16, pk + 8);
-                    }
-                }
-                l = l * alpha + ((a0 + a1) + (a2 + a3));
-                if (!use_bound && t != 0) {
-                    // O may be rescaled only once PV of the item's previous tile is done
-                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_PVDONE), n_pv & 1, SITE_SOFT_O)))) break;
-                    ++n_pv;
-                    tc_fence_after();
-                    if (__any_sync(0xffffffffu, m_new > m2)) {
-                        // running max moved: rescale the row's accumulator
-                        const uint32_t tO = tbase + lane_off + C::T_O;
-#pragma unroll 1
-                        for (int c = 0; c < D / 16; ++c) {
-                            float o[16];
-                            tmem_ld_x16(tO + 16 * c, o);
-                            tmem_ld_wait();
+                        tmem_st_x8(tS + 32 * hh, pk);
+                        if (two) {
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                reg_fence(o[e]);
-                                o[e] *= alpha;
+                            for (int i = 16; i < 32; i += 4) {
+                                a0 += s[i];
+                                a1 += s[i + 1];
+                                a2 += s[i + 2];
+                                a3 += s[i + 3];
                             }
-                            tmem_st_x16(tO + 16 * c, o);
+                            tmem_st_x8(tS + 32 * hh + 16, pk + 8);
                         }
+                }
+                l += (a0 + a1) + (a2 + a3);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cnt(bar(C::B_PFULL + buf), 3);
+                if (pv_flags >= 0) {
+                    if (!(ok = epilogue())) break;
+                    pv_flags = -1;
+                }
+                }
+            } else {
+                for (int t = 0; t < n; ++t) {
+                    const int g = g0 + t;
+                    const int width = t == n0 - 1 ? w0 : (t == n - 1 ? w1 : p.NK);
+                    const int nch = width / 16;
+                    const int buf = g & (kNBuf - 1);
+                    const uint32_t tS = tbase + lane_off + C::t_s(buf);
+                    const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
+                    // the vote keeps the warp converged for the warp-collective TMEM accesses
+                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
+                        break;
+                    tc_fence_after();
+                    // Running max, shared by all groups: this warp's chunks are c = group and
+                    // group + 3.  The groups exchange their tile maxima; the exponentials use a
+                    // reference m2 that moves only when the row max passes it by more than 8 (so
+                    // every p stays below 2^8), and only then is the row's accumulator rescaled.
+                    const bool has0 = group < nch, has1 = group + 3 < nch;
+                    float s[32];
+                    uint32_t pk[16];
+                    if (has0) tmem_ld_x16(tS + 16 * group, s);
+                    if (has1) tmem_ld_x16(tS + 16 * (group + 3), s + 16);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) reg_fence(s[i]);
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                    if (has0) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
+                }
+                if (has1) {
+#pragma unroll
+                    for (int e = 16; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
+                }
+                // exchange slots double-buffered by parity: a warp writes exchange n + 2's slot
+                // only after every partner has written n + 1's, i.e. after it read n's
+                const uint32_t mcount = sbase + C::MISC_OFF + 24u + 4u * quarter;
+                const uint32_t ms = sbase + C::MMAX_OFF + (n_mx & 1) * (kGroups * 128 * 4) + 4u * row;
+                st_shared_f32(ms + 512 * group, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                __syncwarp();
+                if (lane == 0) red_release_shared_add(mcount, 1u);
+                ++n_mx;
+                if (!(ok = __all_sync(0xffffffffu, wt.counter(p, mcount, kGroups * n_mx, SITE_SOFT_X)))) break;
+                float tmax = ld_shared_f32(ms);
+#pragma unroll
+                for (int j = 1; j < kGroups; ++j) tmax = fmaxf(tmax, ld_shared_f32(ms + 512 * j));
+                const float m_tile = tmax * c2;
+                mt = fmaxf(mt, m_tile);
+                float alpha = 1.0f;
+                if (t == 0) {
+                    m2 = m_tile;  // O and l start from zero: nothing to rescale
+                } else if (__any_sync(0xffffffffu, m_tile > m2 + 8.0f)) {
+                    // O may be rescaled only once PV of the item's previous tile is done
+                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_BFREE + ((g - 1) & (kNBuf - 1))),
+                                                              ((g - 1) >> 2) & 1, SITE_SOFT_O))))
+                        break;
+                    tc_fence_after();
+                    const float m_new = m_tile > m2 + 8.0f ? m_tile : m2;
+                    alpha = ex2(m2 - m_new);
+                    m2 = m_new;
+                    // this warp's share of the row's accumulator (the epilogue's column split)
+                    constexpr int NCHO = D / 16;
+                    const int cb = group * NCHO / kGroups, ce = (group + 1) * NCHO / kGroups;
+                    const uint32_t tO = tbase + lane_off + C::T_O;
+#pragma unroll 1
+                    for (int c = cb; c < ce; ++c) {
+                        float o[16];
+                        tmem_ld_x16(tO + 16 * c, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            reg_fence(o[e]);
+                            o[e] *= alpha;
+                        }
+                        tmem_st_x16(tO + 16 * c, o);
                     }
                 }
-                m2 = m_new;
+                const float nb2 = -m2;
+                float a0 = 0.0f, a1 = 0.0f;
+                if (has0) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                    for (int i = 0; i < 16; i += 2) {
+                        a0 += s[i];
+                        a1 += s[i + 1];
+                    }
+                    tmem_st_x8(tS + 16 * group, pk);
+                }
+                if (has1) {
+#pragma unroll
+                    for (int i = 16; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+#pragma unroll
+                    for (int i = 8; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+#pragma unroll
+                    for (int i = 16; i < 32; i += 2) {
+                        a0 += s[i];
+                        a1 += s[i + 1];
+                    }
+                    tmem_st_x8(tS + 16 * (group + 3), pk + 8);
+                }
+                l = l * alpha + (a0 + a1);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -739,11 +799,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (!(ok = epilogue())) break;
                     pv_flags = -1;
                 }
+                }
             }
             if (!ok) break;
             pv_flags = flags | (local << 9);
             pv_b = b_nat;
             pv_m2 = m2;
+            pv_mt = mt;
             pv_l = l;
             pv_grow = grow;
             g0 += n;
