@@ -29,7 +29,8 @@ FSA_ERR_SCRATCH_LIMIT = -5
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
            "fsa_plan_set_center_keys",
            "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_prep", "fsa_norms_noalloc",
-           "fsa_last_cuda_error", "fsa_status_string", "fsa_selftest_wait_timeout")
+           "fsa_last_cuda_error", "fsa_status_string", "fsa_selftest_wait_timeout",
+           "fsa_selftest_grid_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -81,6 +82,8 @@ def load():
             lib.fsa_status_string.restype = ctypes.c_char_p
             lib.fsa_selftest_wait_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int32), vp]
             lib.fsa_selftest_wait_timeout.restype = i32
+            lib.fsa_selftest_grid_timeout.argtypes = [ctypes.c_longlong, i32, i32, ctypes.POINTER(ctypes.c_int32), vp]
+            lib.fsa_selftest_grid_timeout.restype = i32
             _lib = lib
     return _lib
 
@@ -318,3 +321,12 @@ def selftest_wait_timeout(limit_cycles: int, stream=None) -> int:
     _check("fsa_selftest_wait_timeout",
            load().fsa_selftest_wait_timeout(int(limit_cycles), ctypes.byref(status), _stream_handle(stream)))
     return int(status.value)
+
+
+def selftest_grid_timeout(limit_cycles: int, ctas: int, missing: int, stream=None) -> dict:
+    """Run the bounded grid-barrier self test; returns the kernel's report."""
+    res = (ctypes.c_int32 * 4)()
+    _check("fsa_selftest_grid_timeout",
+           load().fsa_selftest_grid_timeout(int(limit_cycles), int(ctas), int(missing), res,
+                                            _stream_handle(stream)))
+    return {"status": int(res[0]), "site": int(res[1]), "gave_up": int(res[2]), "arrived": int(res[3])}

@@ -738,4 +738,27 @@ int fsa_selftest_wait_timeout(long long limit_cycles, int32_t* status, void* str
     return rc;
 }
 
+int fsa_selftest_grid_timeout(long long limit_cycles, int ctas, int missing, int32_t* result, void* stream)
+{
+    if (!result || limit_cycles <= 0 || ctas < 1 || (missing != 0 && missing != 1)) return FSA_ERR_INVALID_ARG;
+    int rc = check_device();
+    if (rc != FSA_OK) return rc;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return FSA_ERR_CUDA;
+    if (ctas > sms) return FSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* d = nullptr;
+    if (cudaMalloc(&d, 8 * sizeof(int)) != cudaSuccess) return FSA_ERR_CUDA;
+    rc = cuda_status(cudaMemsetAsync(d, 0, 8 * sizeof(int), st));
+    if (rc == FSA_OK &&
+        fsa::launch_selftest_grid(limit_cycles, ctas, missing, reinterpret_cast<unsigned*>(d + 4), d, st) != 0)
+        rc = FSA_ERR_CUDA;
+    if (rc == FSA_OK) rc = cuda_status(cudaMemcpyAsync(result, d, 4 * sizeof(int), cudaMemcpyDeviceToHost, st));
+    if (rc == FSA_OK) rc = cuda_status(cudaStreamSynchronize(st));
+    cudaFree(d);
+    return rc;
+}
+
 }  // extern "C"

@@ -54,6 +54,8 @@ int launch_status();
 int launch_attention(const AttnLaunch& L);
 int attn_smem_bytes(int D);
 int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);
+int launch_selftest_grid(long long limit, int ctas, int missing, unsigned* d_counter, int* d_result,
+                         cudaStream_t stream);
 
 struct NormsLaunch {
     const uint16_t* q;

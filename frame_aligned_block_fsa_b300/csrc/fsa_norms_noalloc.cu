@@ -1,16 +1,19 @@
 // fsa_norms_noalloc.cu -- fsa_norms for callers that must not allocate device memory.
 //
 // fsa_norms keeps its scratch (per-frame key sums, per-head gap maxima) in a plan-owned
-// workspace that it grows with cudaMalloc.  Some callers cannot allow that: code that runs
-// while a CUDA graph is being captured, engines that own the whole device memory budget and
-// hand every buffer out themselves, and latency-critical loops that cannot afford the device
-// synchronisation cudaMalloc/cudaFree imply.  fsa_norms_noalloc runs the same three kernels
-// with that scratch in one file-scope device array of fixed size instead.
+// workspace that it grows with cudaMalloc.  Some callers cannot allow that: engines that own the
+// whole device memory budget and hand every buffer out themselves, and loops that cannot take
+// the device synchronisation cudaMalloc/cudaFree imply.  fsa_norms_noalloc runs the same kernels
+// with that scratch in one file-scope device array of fixed size instead, and reads no host
+// buffer: the plan's key runs reach the array as kernel arguments of a small fill kernel.
 //
 // The array is part of the library image: every GPU that loads the library holds it
 // (kNoAllocScratchBytes) until the process exits.  Host code cannot use the array's name as a
 // device address (on the host it names a host-side stand-in), so the first call on each device
-// looks the address up with cudaGetSymbolAddress, with that device current, and caches it.
+// looks the address up with cudaGetSymbolAddress, with that device current, and caches it with
+// the CUDA context it belongs to; a call in another context (after a device reset, say) looks it
+// up again.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstddef>
@@ -30,6 +33,36 @@ static __device__ __align__(256) unsigned char g_norms_scratch[kNoAllocScratchBy
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+// Words of the plan's key runs passed by value to one fill launch (within the 4 KB of kernel
+// arguments).
+constexpr int kFillWords = 960;
+struct FillArgs {
+    int32_t w[kFillWords];
+};
+
+__global__ void fill_runs_kernel(int32_t* dst, int count, const FillArgs a)
+{
+    for (int i = threadIdx.x; i < count; i += blockDim.x) dst[i] = a.w[i];
+}
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+// The driver's cuCtxGetCurrent, reached through the runtime (the library links no libcuda).
+CtxGetCurrentFn ctx_get_current()
+{
+    static CtxGetCurrentFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<CtxGetCurrentFn>(p);
+    });
+    return fn;
+}
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -44,11 +77,17 @@ int scratch_on_current_device(void** out)
         cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
         return FSA_ERR_CUDA;
     if (major != 10 || minor != 3) return FSA_ERR_UNSUPPORTED;
+    // make sure the device's context exists and is current, then read it
+    if (cudaFree(nullptr) != cudaSuccess) return FSA_ERR_CUDA;
+    CtxGetCurrentFn get = ctx_get_current();
+    CUcontext ctx = nullptr;
+    if (!get || get(&ctx) != CUDA_SUCCESS || ctx == nullptr) return FSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    if (g_scratch_addr[dev] == nullptr || g_scratch_ctx[dev] != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_norms_scratch) != cudaSuccess || p == nullptr) return FSA_ERR_CUDA;
         g_scratch_addr[dev] = p;
+        g_scratch_ctx[dev] = ctx;
     }
     *out = g_scratch_addr[dev];
     return FSA_OK;
@@ -89,12 +128,19 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     if (rc != FSA_OK) return rc;
     unsigned char* s = static_cast<unsigned char*>(base);
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The previous call's contents are overwritten: the tickets are zeroed and the runs copied
-    // here, the key sums are written by the first kernel, and the gap maxima are zeroed by the
-    // first kernel before the second max-reduces.
+    // The previous call's contents are overwritten: the tickets are zeroed and the runs written
+    // here (by value, no host buffer is read on the stream), the key sums are written by the
+    // first kernel, and the gap maxima are zeroed by the first kernel before the second
+    // max-reduces.
     if (cudaMemsetAsync(s, 0, tickets_bytes, st) != cudaSuccess) return FSA_ERR_CUDA;
-    if (cudaMemcpyAsync(s + off_runs, pv.runs, runs_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
-        return FSA_ERR_CUDA;
+    const int words = pv.F * fsa::kRunStride;
+    for (int w0 = 0; w0 < words; w0 += fsa::kFillWords) {
+        fsa::FillArgs a;
+        const int cnt = words - w0 < fsa::kFillWords ? words - w0 : fsa::kFillWords;
+        for (int i = 0; i < cnt; ++i) a.w[i] = pv.runs[w0 + i];
+        fsa::fill_runs_kernel<<<1, 256, 0, st>>>(reinterpret_cast<int32_t*>(s + off_runs) + w0, cnt, a);
+        if (cudaGetLastError() != cudaSuccess) return FSA_ERR_CUDA;
+    }
 
     fsa::NormsLaunch L;
     L.q = q;

@@ -619,6 +619,42 @@ static int launch_prep_d(const PrepLaunch& L)
     return launch_status();
 }
 
+// Grid-barrier self test: every CTA meets at the prep kernel's grid barrier, whose target is
+// the CTA count plus `missing`.  With missing = 0 the barrier opens; with missing = 1 it never
+// does, and each CTA's waiting thread must give up after `limit` cycles, raise its CTA's abort
+// flag and record FSA_ERR_TIMEOUT with the grid-barrier site.  result: [status, site, CTAs that
+// saw their abort flag raised, arrivals counted].
+__global__ void __launch_bounds__(256) fsa_selftest_grid_kernel(unsigned* counter, unsigned missing, long long limit,
+                                                                int* result)
+{
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) abort_flag = 0;
+    __syncthreads();
+    WaitCtl wc;
+    wc.abort = &abort_flag;
+    wc.err_word = result + 0;
+    wc.err_site = result + 1;
+    wc.limit = limit;
+    grid_sync(counter, gridDim.x + missing, static_cast<int>(threadIdx.x), wc);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        if (abort_flag) atomicAdd(result + 2, 1);
+        if (blockIdx.x == 0) atomicMax(result + 3, static_cast<int>(ld_acquire_gpu(counter)));
+    }
+}
+
+int launch_selftest_grid(long long limit, int ctas, int missing, unsigned* d_counter, int* d_result,
+                         cudaStream_t stream)
+{
+    unsigned miss = static_cast<unsigned>(missing);
+    void* args[] = {&d_counter, &miss, &limit, &d_result};
+    // cooperative: every CTA is resident, as in the prep kernel, so an open barrier opens
+    if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fsa_selftest_grid_kernel), dim3(ctas), dim3(256),
+                                    args, 0, stream) != cudaSuccess)
+        return -3;
+    return launch_status();
+}
+
 int launch_prep(const PrepLaunch& L)
 {
     if (L.D == 128) return launch_prep_d<128>(L);

@@ -10,6 +10,9 @@ Recipes (the pages measure on production data, which is not available):
           V is N(0, 1).
   offset: as normal, then one vector m_h ~ N(0, 4^2 I_D) per head is added to every key
           of head h (a large component that all keys share).
+  loose:  as normal, then the keys of head h are scaled by 3 + 0.5 (h mod 4): the logits
+          spread out, and the norm bound sits 20 to 60 nats above the row max while the head
+          still passes the gap test at a raised tau (a loose but eligible bound).
   prep:   hidden states x ~ N(0, 1) [N][d_model] and projection weights
           w ~ N(0, 1/d_model) [3 H D][d_model], drawn in that order (make_prep_inputs).
 All draws come from one CPU torch.Generator seeded with the workload's seed, in
@@ -47,6 +50,9 @@ def make_qkv(H: int, N: int, D: int, seed: int, kind: str = "normal"):
     elif kind == "offset":
         m = torch.randn((H, 1, D), generator=g, dtype=torch.float32).mul_(KEY_OFFSET_STD)
         k.add_(m)
+    elif kind == "loose":
+        scale = torch.tensor([3.0 + 0.5 * (h % 4) for h in range(H)], dtype=torch.float32).view(H, 1, 1)
+        k.mul_(scale)
     elif kind != "normal":
         raise ValueError(f"unknown input kind {kind!r}")
     return (q.to(torch.bfloat16).contiguous(), k.to(torch.bfloat16).contiguous(),

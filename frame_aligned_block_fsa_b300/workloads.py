@@ -20,8 +20,9 @@ class Workload:
     w: int          # window half-width in frames
     ref: int        # global reference frame
     block: int      # plan block size: a multiple of 16 dividing T
-    kind: str       # "normal" (i.i.d. N(0,1)), "stress" (log-normal row norms + outlier keys) or
-                    # "offset" (keys share one large per-head component)
+    kind: str       # "normal" (i.i.d. N(0,1)), "stress" (log-normal row norms + outlier keys),
+                    # "offset" (keys share one large per-head component) or "loose" (keys scaled
+                    # per head: loose but eligible bounds)
     seed: int
 
     @property
@@ -41,6 +42,9 @@ WORKLOADS = {
     "sr28k_h8": Workload("sr28k_h8", F=24, T=1200, H=8, D=128, w=2, ref=0, block=80, kind="normal", seed=5),
     # sr28k shapes with a shared key component: the case mean-centred keys are for
     "offset": Workload("offset", F=24, T=1200, H=24, D=128, w=2, ref=0, block=80, kind="offset", seed=6),
+    # small enough for full-row parity, with keys scaled per head so that the bound sits 20-60
+    # nats above the row max: the norm-bound path on loose but eligible bounds (tau 80)
+    "loose": Workload("loose", F=6, T=256, H=4, D=128, w=1, ref=0, block=64, kind="loose", seed=7),
 }
 
 # The 28.8k-token workload is the one the throughput target is stated on.

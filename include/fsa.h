@@ -241,21 +241,22 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
  * fsa_norms_noalloc -- fsa_norms for callers that cannot allocate device memory.
  * The pages have no counterpart; this is a service of the library.  fsa_norms keeps its
  * scratch (per-frame key sums, per-head maxima) in a plan workspace grown with cudaMalloc,
- * and its first call uploads the plan's work list.  Code that runs during CUDA graph
- * capture, engines that hand out all device memory themselves, and loops that cannot afford
- * the device synchronisation of cudaMalloc/cudaFree need a call that allocates nothing:
- * this one keeps that scratch in a fixed 2 MiB device array compiled into the library (every
- * GPU that loads the library holds it until the process exits), zeroes its counters and copies
- * the plan's key runs into it on every call (a small memset and host-to-device copy on
- * `stream`).
+ * and its first call uploads the plan's work list.  Engines that hand out all device memory
+ * themselves, and loops that cannot take the device synchronisation of cudaMalloc/cudaFree,
+ * need a call that allocates nothing: this one keeps that scratch in a fixed 2 MiB device array
+ * compiled into the library (every GPU that loads the library holds it until the process
+ * exits).  On every call it zeroes the array's counters (a small memset on `stream`) and writes
+ * the plan's key runs into it with a small kernel that takes them as launch arguments, so no
+ * host buffer is read on the stream.
  *   Arguments and results are those of fsa_norms, except that kmax, bound and eligible are
  *   required (they are the outputs; qnorm may be NULL).
- *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, (H*F + H)*4 + F*9*4 + H*F*D*4 +
+ *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, (H*F + H)*4 + F*5*4 + H*F*D*4 +
  *   H*F*C*D*4 + H*F*C*4 + H*4 + H*D*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
  *   H=24, F=24, T=1200, D=128 uses 1.4 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT
  *   before any device work.
  *   The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   with that device current and remembers it together with the device's CUDA context; a
+ *   later call in a different context (after cudaDeviceReset, for instance) looks it up again.
  *   Every call shares the one array and overwrites what the previous call left there, so
  *   calls whose work overlaps on the GPU (different streams, or different host threads) race;
  *   serialise them.
@@ -282,6 +283,22 @@ const char* fsa_status_string(int status);
  * (FSA_ERR_TIMEOUT when the wait gave up as designed).  Synchronises the stream.
  */
 int fsa_selftest_wait_timeout(long long limit_cycles, int32_t* status, void* stream);
+
+/*
+ * fsa_selftest_grid_timeout -- checks the bounded grid barrier of fsa_prep without faulting
+ * the GPU.  Launches `ctas` CTAs of 256 threads (cooperatively, so all are resident; 1 <= ctas
+ * <= the SM count) that meet at the same bounded grid barrier fsa_prep uses between its phases,
+ * with a target of ctas + missing arrivals.
+ *   missing = 0: the barrier opens; result = {0, 0, 0, ctas}.
+ *   missing = 1: the barrier never opens; each CTA's waiting thread gives up after limit_cycles
+ *   SM clock cycles and raises its CTA's abort flag, and the kernel reports
+ *   result = {FSA_ERR_TIMEOUT, 16 (the grid-barrier site), ctas, ctas}.
+ *   result (host, 4 int32): status reported by the kernel, wait site, CTAs whose abort flag was
+ *   raised, arrivals counted at the barrier.  Synchronises the stream.
+ *   Errors: FSA_ERR_INVALID_ARG for a NULL result, limit_cycles <= 0, missing not 0 or 1, or
+ *   ctas out of range.
+ */
+int fsa_selftest_grid_timeout(long long limit_cycles, int ctas, int missing, int32_t* result, void* stream);
 
 #ifdef __cplusplus
 }

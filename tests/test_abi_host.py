@@ -189,3 +189,12 @@ def test_prep_rejects_bad_arguments_before_device_work(lib):
         assert call() == fsa.FSA_ERR_UNSUPPORTED              # centred keys: norms pass only
     assert lib.fsa_prep(fake, fake, 256, 2, 128, None, fake, fake, fake, None, None, None, None, None,
                         None) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_grid_selftest_rejects_bad_arguments_before_device_work():
+    lib = fsa.load()
+    res = (ctypes.c_int32 * 4)()
+    assert lib.fsa_selftest_grid_timeout(1000, 2, 1, None, None) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_selftest_grid_timeout(0, 2, 1, res, None) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_selftest_grid_timeout(1000, 0, 1, res, None) == fsa.FSA_ERR_INVALID_ARG
+    assert lib.fsa_selftest_grid_timeout(1000, 2, 2, res, None) == fsa.FSA_ERR_INVALID_ARG

@@ -1,18 +1,17 @@
 """fsa_norms_noalloc: the norms entry point for callers that cannot allocate device memory.
 
-fsa_norms grows a plan workspace with cudaMalloc; callers that run under CUDA graph capture,
-that own the whole device memory budget, or that cannot take the device synchronisation of
-cudaMalloc/cudaFree use fsa_norms_noalloc instead, which keeps its scratch in a fixed array
-inside the library.  These tests check that it gives the same results as fsa_norms on two
-different problems called one after the other (the second call must not see the first call's
-leftovers), that it allocates no device memory, and that it refuses problems larger than its
-scratch before doing any device work.
+fsa_norms grows a plan workspace with cudaMalloc; callers that own the whole device memory
+budget, or that cannot take the device synchronisation of cudaMalloc/cudaFree, use
+fsa_norms_noalloc instead, which keeps its scratch in a fixed array inside the library.  These
+tests check that it gives bit-identical results to fsa_norms (the same kernels run in the same
+order on the same inputs) on two different problems called one after the other (the second call
+must not see the first call's leftovers), that it allocates no device memory, and that it
+refuses problems larger than its scratch before doing any device work.
 
 This file is named so that pytest collects it after every other test file.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
@@ -65,9 +64,8 @@ def test_noalloc_matches_fsa_norms_on_two_calls_in_a_row():
         return qn, km, bd, el
 
     def check(i, got):
-        for name, a, b in zip(("qnorm", "kmax", "bound"), got[:3], refs[i][:3]):
-            np.testing.assert_allclose(a.cpu().numpy(), b.cpu().numpy(), rtol=2e-6, atol=0, err_msg=name)
-        assert torch.equal(got[3].cpu(), refs[i][3].cpu())
+        for name, a, b in zip(("qnorm", "kmax", "bound", "eligible"), got, refs[i]):
+            assert torch.equal(a, b), name
 
     first = call_noalloc(0, bufs[0])   # first call on this device: looks up the scratch address
     torch.cuda.synchronize()
