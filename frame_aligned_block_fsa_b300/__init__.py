@@ -13,11 +13,12 @@ The library is loaded lazily on first use; importing the package needs no GPU.
 """
 from ._lib import (FSA_ERR_CUDA, FSA_ERR_INVALID_ARG, FSA_ERR_SCRATCH_LIMIT, FSA_ERR_TIMEOUT,  # noqa: F401
                    FSA_ERR_UNSUPPORTED, FSA_OK,
-                   FsaError, Plan, forward, forward_ex, forward_host, load, new_stats, norms, norms_noalloc, prep,
+                   FsaError, Plan, forward, forward_ex, forward_host, forward_masked, load, new_stats, norms, norms_noalloc, prep,
                    read_stats,
                    selftest_grid_timeout, selftest_wait_timeout, status_string)
 
-__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "forward_host", "prep", "new_stats",
+__all__ = ["Plan", "norms", "norms_noalloc", "forward", "forward_ex", "forward_host", "forward_masked", "prep",
+           "new_stats",
            "read_stats",
            "selftest_wait_timeout", "selftest_grid_timeout",
            "status_string", "load", "FsaError"]

@@ -28,7 +28,7 @@ FSA_ERR_SCRATCH_LIMIT = -5
 # Exported symbols, in the order include/fsa.h declares them.
 SYMBOLS = ("fsa_plan", "fsa_plan_destroy", "fsa_plan_export", "fsa_plan_set_tau", "fsa_plan_set_key_tile",
            "fsa_plan_set_center_keys",
-           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_prep", "fsa_norms_noalloc",
+           "fsa_norms", "fsa_forward", "fsa_forward_ex", "fsa_forward_host", "fsa_forward_masked", "fsa_prep", "fsa_norms_noalloc",
            "fsa_last_cuda_error", "fsa_status_string", "fsa_selftest_wait_timeout",
            "fsa_selftest_grid_timeout")
 
@@ -72,6 +72,8 @@ def load():
             lib.fsa_forward_ex.restype = i32
             lib.fsa_forward_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, i32, vp]
             lib.fsa_forward_host.restype = i32
+            lib.fsa_forward_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, vp, i32, vp, vp]
+            lib.fsa_forward_masked.restype = i32
             lib.fsa_prep.argtypes = [vp, vp, i32, i32, i32, vp] + [vp] * 9
             lib.fsa_prep.restype = i32
             lib.fsa_norms_noalloc.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp]
@@ -313,6 +315,22 @@ def forward_ex(q, k, v, plan: Plan, mode: str = "norm_bound", out=None, lse=None
     _check("fsa_forward_ex", load().fsa_forward_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), H, D,
                                                    plan.handle, MODES[mode], _ptr(bound), _ptr(eligible),
                                                    _ptr(rowmax), _ptr(stats), st))
+    return out, lse
+
+
+def forward_masked(q, k, v, plan: Plan, block: int = 128, out=None, lse=None, stats=None, stream=None):
+    """fsa_forward_masked: the masked-block comparison variant (blocks of `block` tokens over the
+    padded sequence, mask predicates, window and reference passes plus a merge)."""
+    import torch
+
+    H, N, D = _check_qkv(plan, q, k, v)
+    if out is None:
+        out = torch.empty((H, N, D), dtype=torch.float32, device=q.device)
+    if lse is None:
+        lse = torch.empty((H, N), dtype=torch.float32, device=q.device)
+    _check("fsa_forward_masked", load().fsa_forward_masked(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), H, D,
+                                                           plan.handle, int(block), _ptr(stats),
+                                                           _stream_handle(stream)))
     return out, lse
 
 

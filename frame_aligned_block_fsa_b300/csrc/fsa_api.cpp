@@ -65,6 +65,15 @@ struct fsa_plan_s {
     float* d_hlse = nullptr;
     cudaStream_t s_in = nullptr, s_comp = nullptr, s_out = nullptr;
     std::vector<cudaEvent_t> ev;                     // [2 * chunks + 1]
+    // fsa_forward_masked: item tables of the last block size used (window pass, reference
+    // pass) and the reference pass's results
+    int mask_block = 0;
+    int mask_n_win = 0, mask_n_ref = 0;              // items per head
+    int32_t* d_mask_win = nullptr;
+    int32_t* d_mask_ref = nullptr;
+    int64_t cap_out2 = 0, cap_lse2 = 0;
+    float* d_out2 = nullptr;
+    float* d_lse2 = nullptr;
 };
 
 namespace {
@@ -269,6 +278,7 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
     fsa::AttnLaunch L;
     L.D = D;
     L.H = H;
+    L.masked = false;
     L.sms = P->sms;
     L.tmQ = &mq;
     L.tmK = &mk;
@@ -276,6 +286,7 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
     L.stream = st;
     fsa::AttnParams& a = L.params;
     a.runs = P->d_runs;
+    a.n_tab = P->F;
     a.F = P->F;
     a.T = P->T;
     a.N = static_cast<int>(P->N);
@@ -292,8 +303,40 @@ int forward_locked(fsa_plan_s* P, const uint16_t* q, const uint16_t* k, const ui
     a.rowmax = rowmax;
     a.stats = dev_stats;
     a.wait_limit = kDefaultWaitLimit;
+    a.mask_w = a.mask_ref = a.mask_pass = 0;
     rc = fsa::launch_attention(L);
     return rc == 0 ? FSA_OK : (rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA);
+}
+
+// Work items of the masked block variant with blocks of B tokens, one table per pass, the same
+// for every head.  Query and key blocks of B tokens tile the sequence padded to a multiple of B.
+// A query block takes every key block that meets the union of its rows' key intervals: the
+// windows of its frames (one interval, pass 0) and, when the window of at least one of its
+// frames leaves it out, the reference frame (pass 1).  Each 128-row tile of a query block that
+// holds a real row is one item: [first row, first key, keys, 0, 0].
+void masked_items(const fsa_plan_s* P, int B, std::vector<int32_t>& win, std::vector<int32_t>& refp)
+{
+    const int64_t N = P->N, T = P->T, F = P->F, w = P->w, r = P->ref;
+    win.clear();
+    refp.clear();
+    const int64_t r0 = (r * T / B) * B, r1 = ((r + 1) * T + B - 1) / B * B;
+    for (int64_t q0 = 0; q0 < N; q0 += B) {
+        const int64_t q1 = std::min<int64_t>(N, q0 + B);
+        const int64_t fa = q0 / T, fb = (q1 - 1) / T;
+        const int64_t lo = std::max<int64_t>(0, fa - w), hi = std::min<int64_t>(F - 1, fb + w);
+        const int64_t k0 = (lo * T / B) * B, k1 = ((hi + 1) * T + B - 1) / B * B;
+        const bool need_ref = !(fb - w <= r && r <= fa + w);
+        for (int64_t t0 = q0; t0 < q1; t0 += 128) {
+            const int32_t a[kRunStride] = {static_cast<int32_t>(t0), static_cast<int32_t>(k0),
+                                           static_cast<int32_t>(k1 - k0), 0, 0};
+            win.insert(win.end(), a, a + kRunStride);
+            if (need_ref) {
+                const int32_t b[kRunStride] = {static_cast<int32_t>(t0), static_cast<int32_t>(r0),
+                                               static_cast<int32_t>(r1 - r0), 0, 0};
+                refp.insert(refp.end(), b, b + kRunStride);
+            }
+        }
+    }
 }
 
 constexpr float kPrepEps = 1e-6f;           // RMS-norm epsilon
@@ -516,6 +559,10 @@ void fsa_plan_destroy(fsa_plan_t plan)
         cudaFree(plan->d_hv);
         cudaFree(plan->d_hout);
         cudaFree(plan->d_hlse);
+        cudaFree(plan->d_mask_win);
+        cudaFree(plan->d_mask_ref);
+        cudaFree(plan->d_out2);
+        cudaFree(plan->d_lse2);
         for (cudaStream_t s : {plan->s_in, plan->s_comp, plan->s_out})
             if (s) cudaStreamDestroy(s);
         for (cudaEvent_t e : plan->ev) cudaEventDestroy(e);
@@ -652,6 +699,87 @@ int fsa_forward_ex(const uint16_t* q, const uint16_t* k, const uint16_t* v, floa
     if ((rc = ensure_device(plan)) != FSA_OK) return rc;
     if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
     return forward_locked(plan, q, k, v, out, lse, H, D, NK, mode, bound, eligible, rowmax, dev_stats, st);
+}
+
+int fsa_forward_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H,
+                       int D, fsa_plan_t plan, int block, fsa_stats_t* dev_stats, void* stream)
+{
+    int rc = check_shape(plan, H, D);
+    if (rc != FSA_OK) return rc;
+    if (block < 128 || block > 1024 || block % 128 != 0) return FSA_ERR_INVALID_ARG;
+    if (H == 0) return FSA_OK;
+    if (!q || !k || !v || !out || !lse) return FSA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return FSA_ERR_INVALID_ARG;
+    // the padded key range of the last query block must stay inside int32 token indices
+    if ((plan->N + block) * static_cast<int64_t>(H) >= (int64_t(1) << 31)) return FSA_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    std::lock_guard<std::mutex> lock(plan->mu);
+    if ((rc = ensure_device(plan)) != FSA_OK) return rc;
+    if (plan->mask_block != block) {
+        std::vector<int32_t> win, refp;
+        masked_items(plan, block, win, refp);
+        cudaFree(plan->d_mask_win);
+        cudaFree(plan->d_mask_ref);
+        plan->d_mask_win = plan->d_mask_ref = nullptr;
+        plan->mask_block = 0;
+        if ((rc = upload(&plan->d_mask_win, win)) != FSA_OK || (rc = upload(&plan->d_mask_ref, refp)) != FSA_OK)
+            return rc;
+        plan->mask_n_win = static_cast<int>(win.size() / kRunStride);
+        plan->mask_n_ref = static_cast<int>(refp.size() / kRunStride);
+        plan->mask_block = block;
+    }
+    const int64_t rows = static_cast<int64_t>(H) * plan->N;
+    if (plan->mask_n_ref > 0) {
+        if ((rc = grow(&plan->d_out2, &plan->cap_out2, rows * D)) != FSA_OK) return rc;
+        if ((rc = grow(&plan->d_lse2, &plan->cap_lse2, rows)) != FSA_OK) return rc;
+    }
+    if (dev_stats && (rc = cuda_status(cudaMemsetAsync(dev_stats, 0, sizeof(fsa_stats_t), st))) != FSA_OK) return rc;
+    CUtensorMap mq, mk, mv;
+    if ((rc = make_tensor_map(&mq, q, rows, D, 128)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mk, k, rows, D, fsa::kMaxKeyTile)) != FSA_OK) return rc;
+    if ((rc = make_tensor_map(&mv, v, rows, D, fsa::kMaxKeyTile)) != FSA_OK) return rc;
+    for (int pass = 0; pass < 2; ++pass) {
+        const int n_items = pass == 0 ? plan->mask_n_win : plan->mask_n_ref;
+        if (n_items == 0) continue;
+        fsa::AttnLaunch L;
+        L.D = D;
+        L.H = H;
+        L.masked = true;
+        L.sms = plan->sms;
+        L.tmQ = &mq;
+        L.tmK = &mk;
+        L.tmV = &mv;
+        L.stream = st;
+        fsa::AttnParams& a = L.params;
+        a.runs = pass == 0 ? plan->d_mask_win : plan->d_mask_ref;
+        a.n_tab = n_items;
+        a.F = plan->F;
+        a.T = plan->T;
+        a.N = static_cast<int>(plan->N);
+        a.n_qt = 1;
+        a.per_head = n_items;
+        a.total = H * n_items;
+        a.NK = fsa::kMaxKeyTile;
+        a.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(D)));
+        a.mode = FSA_MODE_ONLINE_MAX;
+        a.bound = nullptr;
+        a.eligible = nullptr;
+        a.out = pass == 0 ? out : plan->d_out2;
+        a.lse = pass == 0 ? lse : plan->d_lse2;
+        a.rowmax = nullptr;
+        a.stats = dev_stats;
+        a.wait_limit = kDefaultWaitLimit;
+        a.mask_w = plan->w;
+        a.mask_ref = plan->ref;
+        a.mask_pass = pass;
+        rc = fsa::launch_attention(L);
+        if (rc != 0) return rc == -2 ? FSA_ERR_UNSUPPORTED : FSA_ERR_CUDA;
+    }
+    if (plan->mask_n_ref > 0 &&
+        fsa::launch_masked_merge(out, lse, plan->d_out2, plan->d_lse2, H, static_cast<int>(plan->N), plan->T,
+                                 plan->F, plan->w, plan->ref, D, st) != 0)
+        return FSA_ERR_CUDA;
+    return FSA_OK;
 }
 
 int fsa_forward(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse, int H, int D,

@@ -141,9 +141,11 @@ constexpr float kUnderflowGap = 87.33654475055310898657f;  // 126 ln 2
 
 // The key tiles of one CTA's items, in order.  An item is one 128-row query tile (h, f, qt);
 // its keys are the runs of frame f (at most two: the window and the reference frame when it
-// lies outside the window), cut into tiles of at most NK keys.  The kernel parameters are
-// passed to every call instead of being held, so the iterator costs registers only for its
-// position.
+// lies outside the window), cut into tiles of at most NK keys.  In the masked block variant an
+// item is a 128-row tile of a query block on the padded sequence with one key run, read from
+// its item table.  The kernel parameters are passed to every call instead of being held, so the
+// iterator costs registers only for its position.
+template <bool MASKED>
 struct TileIter {
     int it;                          // current item index
     int local = -1;                  // items of this CTA begun so far, minus one
@@ -162,16 +164,26 @@ struct TileIter {
         ++local;
         h = it / p.per_head;
         const int loc = it - h * p.per_head;
-        const int f = loc / p.n_qt;
-        const int qt = loc - f * p.n_qt;
-        row0 = f * p.T + qt * 128;
-        valid = min(128, p.T - qt * 128);
-        const int32_t* R = runs_tab + f * kRunStride;
-        const int nr = R[0];
-        s0 = R[1];
-        l0 = R[2];
-        s1 = nr > 1 ? R[3] : 0;
-        lt = l0 + (nr > 1 ? R[4] : 0);
+        if constexpr (MASKED) {
+            const int32_t* R = runs_tab + loc * kRunStride;
+            row0 = R[kMaskItemRow];
+            valid = min(128, p.N - row0);
+            s0 = R[kMaskItemKey];
+            l0 = R[kMaskItemLen];
+            s1 = 0;
+            lt = l0;
+        } else {
+            const int f = loc / p.n_qt;
+            const int qt = loc - f * p.n_qt;
+            row0 = f * p.T + qt * 128;
+            valid = min(128, p.T - qt * 128);
+            const int32_t* R = runs_tab + f * kRunStride;
+            const int nr = R[0];
+            s0 = R[1];
+            l0 = R[2];
+            s1 = nr > 1 ? R[3] : 0;
+            lt = l0 + (nr > 1 ? R[4] : 0);
+        }
         pos = 0;
         return true;
     }
@@ -249,7 +261,7 @@ struct AttnWait {
     }
 };
 
-template <int D>
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p)
@@ -266,11 +278,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    // key runs of every frame into shared memory when they fit
-    const bool runs_in_smem = p.F <= kSmemRunFrames;
+    // key runs of every frame (masked variant: the item table) into shared memory when they fit
+    const bool runs_in_smem = p.n_tab <= kSmemRunFrames;
     int32_t* runs_s = reinterpret_cast<int32_t*>(sgen + C::RUNS_OFF);
     if (runs_in_smem)
-        for (int i = threadIdx.x; i < p.F * kRunStride; i += blockDim.x) runs_s[i] = p.runs[i];
+        for (int i = threadIdx.x; i < p.n_tab * kRunStride; i += blockDim.x) runs_s[i] = p.runs[i];
     const int32_t* runs_tab = runs_in_smem ? runs_s : p.runs;
 
     if (threadIdx.x == 0) {
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // a slot is free once the tensor work that read it is done: S(g - 4) for K slot g & 3,
             // PV(g - 4) for V slot g & 3
             const int b_free = is_k ? C::B_SFULL : C::B_BFREE;
-            TileIter it;
+            TileIter<MASKED> it;
             int n = 0, nq = 0;  // tiles and Q tiles issued
             int start, width;
             bool first, last;
@@ -362,7 +374,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // the next tile's barriers go out right after the first MMA of a tile, so their answers
         // are back while the pipe still has that tile's MMAs to run.
         const bool leader = elect_one();
-        TileIter si;
+        TileIter<MASKED> si;
         int nq = 0;  // Q tiles copied into TMEM
         bool ok = true;
         int start, width;
@@ -428,7 +440,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     } else if (warp == kWarpPV) {
         // ------------------------------------------------------------- tcgen05 issuer: PV
         const bool leader = elect_one();
-        TileIter vi;
+        TileIter<MASKED> vi;
         int n_items = 0;
         long long n_pairs = 0;
         bool ok = true;
@@ -502,7 +514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         auto fetch = [&](int item, float& b, int& el) {
             b = 0.0f;
             el = 1;
-            if (item >= p.total) return;
+            if (MASKED || item >= p.total) return;
             const int h = item / p.per_head;
             const int loc = item - h * p.per_head;
             const int f = loc / p.n_qt;
@@ -546,7 +558,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float l_row = ld_shared_f32(ls);
 #pragma unroll
             for (int j = 1; j < kGroups; ++j) l_row += ld_shared_f32(ls + 512 * j);
-            const float inv_l = 1.0f / l_row;
+            // masked variant: a row without keys in this pass has l = 0: out 0, lse -inf
+            const float inv_l = (MASKED && !(l_row > 0.0f)) ? 0.0f : 1.0f / l_row;
             const bool rvalid = row < (pv_flags & 0xff);
             const bool ub = (pv_flags >> 8) & 1;
             if (!__all_sync(0xffffffffu, wt.bar(p, bar(C::B_OFULL), item & 1, SITE_SOFT_O))) return false;
@@ -596,19 +609,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int item = blockIdx.x, local = 0; ok && item < p.total; item += gridDim.x, ++local) {
             const int h = item / p.per_head;
             const int loc = item - h * p.per_head;
-            const int f = loc / p.n_qt;
-            const int qt = loc - f * p.n_qt;
-            // the frame's key runs, cut into tiles of NK keys: n0 tiles of run 0 (the last of
+            // the item's key runs, cut into tiles of NK keys: n0 tiles of run 0 (the last of
             // them w0 keys), then n1 of run 1 (the last w1 keys)
-            const int32_t* R = runs_tab + f * kRunStride;
-            const int l0 = R[2], l1 = R[0] > 1 ? R[4] : 0;
-            const int n0 = (l0 + p.NK - 1) / p.NK, n1 = (l1 + p.NK - 1) / p.NK;
-            const int w0 = l0 - (n0 - 1) * p.NK, w1 = l1 - (n1 - 1) * p.NK;
+            int n0, n1, w0, w1, valid, row0;
+            // masked variant: this row's key interval [ja, jb) and the item's first key
+            int ja = 0, jb = 0, kst = 0;
+            if constexpr (MASKED) {
+                const int32_t* R = runs_tab + loc * kRunStride;
+                row0 = R[kMaskItemRow];
+                kst = R[kMaskItemKey];
+                n0 = R[kMaskItemLen] / p.NK;
+                n1 = 0;
+                w0 = p.NK;
+                w1 = 0;
+                valid = min(128, p.N - row0);
+                if (row < valid) {
+                    const int fi = (row0 + row) / p.T;
+                    const int lo = max(0, fi - p.mask_w), hi = min(p.F - 1, fi + p.mask_w);
+                    if (p.mask_pass == 0) {
+                        ja = lo * p.T;
+                        jb = (hi + 1) * p.T;
+                    } else if (p.mask_ref < lo || p.mask_ref > hi) {
+                        ja = p.mask_ref * p.T;
+                        jb = ja + p.T;
+                    }
+                }
+            } else {
+                const int f = loc / p.n_qt;
+                const int qt = loc - f * p.n_qt;
+                const int32_t* R = runs_tab + f * kRunStride;
+                const int l0 = R[2], l1 = R[0] > 1 ? R[4] : 0;
+                n0 = (l0 + p.NK - 1) / p.NK;
+                n1 = (l1 + p.NK - 1) / p.NK;
+                w0 = l0 - (n0 - 1) * p.NK;
+                w1 = l1 - (n1 - 1) * p.NK;
+                valid = min(128, p.T - qt * 128);
+                row0 = f * p.T + qt * 128;
+            }
             const int n = n0 + n1;
-            const bool use_bound = p.mode == 0 && p.bound != nullptr && nx_el != 0;
-            const int valid = min(128, p.T - qt * 128);
+            const bool use_bound = !MASKED && p.mode == 0 && p.bound != nullptr && nx_el != 0;
             flags = valid | (use_bound ? 1 << 8 : 0);
-            grow = h * p.N + f * p.T + qt * 128 + row;
+            grow = h * p.N + row0 + row;
             b_nat = nx_b;
             fetch(item + static_cast<int>(gridDim.x), nx_b, nx_el);
             m2 = -INFINITY;
@@ -695,7 +736,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const int nch = width / 16;
                     const int buf = g & (kNBuf - 1);
                     const uint32_t tS = tbase + lane_off + C::t_s(buf);
-                    const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
+                    // masked variant: rows past the sequence have an empty key interval instead
+                    const float c2 = (MASKED || row < (flags & 0xff)) ? p.scale_log2 : 0.0f;
                     // the vote keeps the warp converged for the warp-collective TMEM accesses
                     if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
                         break;
@@ -712,6 +754,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) reg_fence(s[i]);
+                    if constexpr (MASKED) {
+                        // mask predicates, on tiles that are not wholly inside the row's interval
+                        const int j0 = kst + t * p.NK;
+                        if (!(j0 >= ja && j0 + width <= jb)) {
+                            const unsigned span = static_cast<unsigned>(jb - ja);
+                            const int c0 = j0 + 16 * group - ja, c1 = j0 + 16 * (group + 3) - ja;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                if (static_cast<unsigned>(c0 + e) >= span) s[e] = -INFINITY;
+                                if (static_cast<unsigned>(c1 + e) >= span) s[16 + e] = -INFINITY;
+                            }
+                        }
+                    }
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
                     if (has0) {
 #pragma unroll
@@ -745,7 +800,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         break;
                     tc_fence_after();
                     const float m_new = m_tile > m2 + 8.0f ? m_tile : m2;
-                    alpha = ex2(m2 - m_new);
+                    // (masked variant: a row with no key yet keeps m2 = -inf and alpha = 1)
+                    alpha = (!MASKED || m_new > m2) ? ex2(m2 - m_new) : 1.0f;
                     m2 = m_new;
                     // this warp's share of the row's accumulator (the epilogue's column split)
                     constexpr int NCHO = D / 16;
@@ -764,7 +820,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tmem_st_x16(tO + 16 * c, o);
                     }
                 }
-                const float nb2 = -m2;
+                // masked variant: m2 = -inf only while every key of the row so far, this tile's
+                // included, is masked; their weights are 2^-inf = 0
+                const float nb2 = (MASKED && m2 == -INFINITY) ? 0.0f : -m2;
                 float a0 = 0.0f, a1 = 0.0f;
                 if (has0) {
 #pragma unroll
@@ -843,11 +901,11 @@ __global__ void fsa_selftest_wait_kernel(long long limit, int* status)
     }
 }
 
-template <int D>
+template <int D, bool MASKED>
 static int launch_attn(const AttnLaunch& L)
 {
     using C = AttnCfg<D>;
-    auto kern = fsa_attn_fwd_kernel<D>;
+    auto kern = fsa_attn_fwd_kernel<D, MASKED>;
     static bool attr_done = false;  // per instantiation
     if (!attr_done) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -874,9 +932,51 @@ int launch_attention(const AttnLaunch& L)
 {
     static_assert(kMaxKeyTile == kBufCols, "one key tile fills an S buffer at most");
     if (L.params.NK < 16 || L.params.NK > kMaxKeyTile || L.params.NK % 16 != 0) return -2;
-    if (L.D == 64) return launch_attn<64>(L);
-    if (L.D == 128) return launch_attn<128>(L);
+    if (L.masked && (L.params.mode != 1 || L.params.bound != nullptr || L.params.NK != kMaxKeyTile)) return -2;
+    if (L.D == 64) return L.masked ? launch_attn<64, true>(L) : launch_attn<64, false>(L);
+    if (L.D == 128) return L.masked ? launch_attn<128, true>(L) : launch_attn<128, false>(L);
     return -2;
+}
+
+// One warp per row of the [H][N] rows.  Rows whose window [f - w, f + w] (clipped) leaves out
+// the reference frame: lse = log(e^lse + e^lse2) and out = e^(lse - lse') out + e^(lse2 - lse')
+// out2; other rows keep the window pass's result.  A reference pass without keys for the row
+// (lse2 = -inf) leaves it unchanged too.
+__global__ void __launch_bounds__(256) masked_merge_kernel(float* __restrict__ out, float* __restrict__ lse,
+                                                           const float* __restrict__ out2,
+                                                           const float* __restrict__ lse2, int64_t rows, int N,
+                                                           int T, int F, int w, int ref, int D)
+{
+    const int64_t r = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (r >= rows) return;
+    const int i = static_cast<int>(r % N);
+    const int f = i / T;
+    if (ref >= max(0, f - w) && ref <= min(F - 1, f + w)) return;
+    const float l1 = lse[r], l2 = lse2[r];
+    if (!(l2 > -INFINITY)) return;
+    const float m = fmaxf(l1, l2);
+    const float e1 = expf(l1 - m), e2 = expf(l2 - m);
+    const float inv = 1.0f / (e1 + e2);
+    const float a1 = e1 * inv, a2 = e2 * inv;
+    float4* o = reinterpret_cast<float4*>(out + r * D);
+    const float4* o2 = reinterpret_cast<const float4*>(out2 + r * D);
+    for (int c = lane; c < D / 4; c += 32) {
+        const float4 x = o[c], y = __ldg(o2 + c);
+        o[c] = make_float4(a1 * x.x + a2 * y.x, a1 * x.y + a2 * y.y, a1 * x.z + a2 * y.z, a1 * x.w + a2 * y.w);
+    }
+    if (lane == 0) lse[r] = m + logf(e1 + e2);
+}
+
+int launch_masked_merge(float* out, float* lse, const float* out2, const float* lse2, int H, int N, int T, int F,
+                        int w, int ref, int D, cudaStream_t stream)
+{
+    const int64_t rows = static_cast<int64_t>(H) * N;
+    if (rows == 0) return 0;
+    const int64_t blocks = (rows + 7) / 8;
+    masked_merge_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(out, lse, out2, lse2, rows, N, T, F, w,
+                                                                          ref, D);
+    return launch_status();
 }
 
 int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream)

@@ -18,11 +18,17 @@ constexpr int kRunStride = 1 + 2 * kMaxRuns;
 // Largest key tile of the attention kernel (its four S buffers hold 64 columns each).
 constexpr int kMaxKeyTile = 64;
 
+// Work item of the masked block variant (one 128-row query tile of a query block on the padded
+// sequence): [first query token, first key token, keys (a multiple of the block size), 0, 0].
+// The kernel reads it from the same table slot as a frame's key runs.
+constexpr int kMaskItemRow = 0, kMaskItemKey = 1, kMaskItemLen = 2;
+
 struct AttnParams {
-    const int32_t* runs;   // [F][kRunStride]
+    const int32_t* runs;   // frame-aligned: [F][kRunStride] key runs; masked: [per_head][kRunStride] items
+    int n_tab;             // entries of `runs` (F, or the masked items per head)
     int F, T, N;           // frames, tokens per frame, tokens per head
-    int n_qt;              // 128-row query tiles per frame, ceil(T / 128)
-    int per_head;          // work items per head, F * n_qt
+    int n_qt;              // 128-row query tiles per frame, ceil(T / 128) (frame-aligned)
+    int per_head;          // work items per head: F * n_qt, or the masked items per head
     int total;             // work items, H * per_head
     int NK;                // keys per tile (multiple of 16, at most kMaxKeyTile)
     float scale_log2;      // c * log2(e)
@@ -34,10 +40,15 @@ struct AttnParams {
     float* rowmax;         // [H][N] or null
     fsa_stats_t* stats;    // or null
     long long wait_limit;  // clock cycles
+    // masked block variant: each row's keys are one interval of the sequence, the window of
+    // frames [f - w, f + w] clipped to [0, F) (pass 0) or the reference frame when outside that
+    // window (pass 1, else no key); keys outside it are masked by predicate
+    int mask_w, mask_ref, mask_pass;
 };
 
 struct AttnLaunch {
     int D, H;
+    bool masked;           // the masked block variant (online softmax only)
     int sms;               // persistent grid: min(sms, work items) CTAs
     const CUtensorMap* tmQ;  // boxes of 128 rows
     const CUtensorMap* tmK;  // boxes of NK rows
@@ -52,6 +63,10 @@ void note_cuda_error(int code);
 int launch_status();
 
 int launch_attention(const AttnLaunch& L);
+// Merge of the masked variant's two passes, in place on (out, lse): rows whose window leaves out
+// the reference frame combine their window-pass result with the reference pass's (out2, lse2).
+int launch_masked_merge(float* out, float* lse, const float* out2, const float* lse2, int H, int N, int T, int F,
+                        int w, int ref, int D, cudaStream_t stream);
 int attn_smem_bytes(int D);
 int launch_selftest_wait(long long limit, int* d_status, cudaStream_t stream);
 int launch_selftest_grid(long long limit, int ctas, int missing, unsigned* d_counter, int* d_result,

@@ -209,6 +209,35 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
                      int H, int D, fsa_plan_t plan, int mode, int heads_per_chunk, void* stream);
 
 /*
+ * fsa_forward_masked -- the same attention, computed the way a general block-sparse kernel
+ * with a mask computes it: the comparison point for the frame-aligned layout.
+ * Source: aihot.vn page above, section "Xoa bo mat na", and the bib.com.ua page "HeyGen
+ * pryskoryla Avatar IV na TPU u 1,86 raza" (its section on the sparse-attention mask): they
+ * describe the state the frame-aligned kernel replaced: blocks of a multiple of 128 tokens over a sequence padded
+ * to a whole number of blocks, element-wise mask predicates on the blocks a frame boundary cuts,
+ * and the window and the reference frame run as two passes whose partial results a third pass
+ * merges.  This entry point does exactly that on B300:
+ *   pass 0: query blocks and key blocks of `block` tokens; a query block visits every key block
+ *     that meets the union of its rows' windows [f - w, f + w] (clipped to [0, F)); keys outside
+ *     a row's own window are masked by predicate on the tiles the interval cuts;
+ *   pass 1: the query blocks that hold a row whose window leaves out the reference frame visit
+ *     the key blocks of the reference frame; rows whose window holds it see no key there;
+ *   merge: rows whose window leaves out the reference frame combine the two softmax results
+ *     through their log-sum-exps; pass 1 writes its fp32 partial out and lse to plan-owned
+ *     buffers (H*N*D + H*N floats, grown on first use).
+ * Both passes run the running-max softmax (the pages' comparison state has no norm bound), on
+ * the same persistent tcgen05 kernel as fsa_forward (128-row query tiles, 64-key tiles).  The
+ * result is the attention fsa_forward computes, up to rounding.
+ *   q, k, v, out, lse, H, D, stream: as fsa_forward.  plan: its F, T, w and ref are used (its
+ *   block size is not).  block: a multiple of 128 from 128 to 1024.  dev_stats: optional, as in
+ *   fsa_forward_ex (items_done and pairs_visited count both passes, masked pairs included).
+ *   The item tables of the last block size used are kept in the plan.
+ * Errors as fsa_forward, plus FSA_ERR_INVALID_ARG for a block size outside that set.
+ */
+int fsa_forward_masked(const uint16_t* q, const uint16_t* k, const uint16_t* v, float* out, float* lse,
+                       int H, int D, fsa_plan_t plan, int block, fsa_stats_t* dev_stats, void* stream);
+
+/*
  * fsa_prep -- the attention's inputs from the hidden states, in one fused pass.
  * Source: aihot.vn page above, "Bo cuc la ABI", Fig. 5: normalisation, rotary embeddings,
  * projection and head packing fused into one kernel that writes exactly the layout the next

@@ -198,3 +198,16 @@ def test_grid_selftest_rejects_bad_arguments_before_device_work():
     assert lib.fsa_selftest_grid_timeout(0, 2, 1, res, None) == fsa.FSA_ERR_INVALID_ARG
     assert lib.fsa_selftest_grid_timeout(1000, 0, 1, res, None) == fsa.FSA_ERR_INVALID_ARG
     assert lib.fsa_selftest_grid_timeout(1000, 2, 2, res, None) == fsa.FSA_ERR_INVALID_ARG
+
+
+def test_masked_variant_rejects_bad_block_sizes_before_device_work():
+    lib = fsa.load()
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the argument checks come first
+    with fsa.Plan(4, 64, 1, 0, 16) as plan:
+        for bad in (0, 64, 200, 1152, -128):
+            rc = lib.fsa_forward_masked(fake, fake, fake, fake, fake, 2, 128, plan.handle, bad, None, None)
+            assert rc == fsa.FSA_ERR_INVALID_ARG, bad
+        rc = lib.fsa_forward_masked(fake, fake, fake, fake, fake, 2, 96, plan.handle, 128, None, None)
+        assert rc == fsa.FSA_ERR_UNSUPPORTED
+        # an empty problem does nothing and touches no pointer
+        assert lib.fsa_forward_masked(None, None, None, None, None, 0, 128, plan.handle, 128, None, None) == fsa.FSA_OK
