@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--sweep", action="store_true",
                     help="instead of the bench line: one JSON line per workload and softmax mode (attention time, "
                          "norms time, bound-gap statistics, fallback heads, underflow rows)")
+    ap.add_argument("--sweep-part", choices=["all", "workloads", "key_tile", "masked"], default="all",
+                    help="with --sweep: every part, or only the workload/mode lines, the key-tile sweep, or the "
+                         "masked-block comparison")
     return ap.parse_args()
 
 
@@ -250,17 +253,131 @@ def reference_arm(args, rank):
     print(json.dumps(line), flush=True)
 
 
+def _timed(fn, reps, stream):
+    """Mean milliseconds of `reps` calls of fn after three untimed ones (CUDA events on `stream`)."""
+    import torch
+
+    for _ in range(3):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
 def sweep(args):
-    """Every workload in both softmax modes, and in norm_bound mode once more with mean-centred
-    keys; one JSON line each (not the bench contract line)."""
+    """One JSON line per measurement (not the bench contract line):
+    workloads -- every workload in both softmax modes, and in norm_bound mode once more with
+                 mean-centred keys;
+    key_tile  -- the attention kernel at key tiles of 16, 32, 48 and 64 keys, both modes, at the
+                 28.8k and 57.6k workloads (the block geometry retuned for the softmax);
+    masked    -- the masked-block comparison variant at blocks of 128, 256 and 512 tokens beside
+                 the frame-aligned kernel in both modes, at the 28.8k, 57.6k and stress workloads."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if args.sweep_part in ("all", "workloads"):
+        sweep_workloads(args, dev)
+    if args.sweep_part in ("all", "key_tile"):
+        sweep_key_tile(args, dev)
+    if args.sweep_part in ("all", "masked"):
+        sweep_masked(args, dev)
+
+
+def sweep_key_tile(args, dev):
     import torch
 
     import frame_aligned_block_fsa_b300 as fsa
     from frame_aligned_block_fsa_b300.inputs import make_workload_inputs
     from frame_aligned_block_fsa_b300.workloads import WORKLOADS
 
-    dev = torch.device("cuda", 0)
-    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    peaks, _ = load_peaks()
+    reps = max(3, min(args.steps, 20))
+    for name in ("sr28k", "sr57k"):
+        wl = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_workload_inputs(wl))
+        H, N, D = wl.H, wl.N, wl.D
+        out = torch.empty((H, N, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((H, N), dtype=torch.float32, device=dev)
+        bound = torch.empty((H, N), dtype=torch.float32, device=dev)
+        elig = torch.empty(H, dtype=torch.uint8, device=dev)
+        with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+            flops = plan.nnz() * 4 * wl.block * wl.block * D * H
+            fsa.norms(q, k, plan, None, None, bound, elig, stream=stream)
+            for key_tile in (16, 32, 48, 64):
+                plan.set_key_tile(key_tile)
+                for mode in ("norm_bound", "online_max"):
+                    ms = _timed(lambda: fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound,
+                                                       eligible=elig, stream=stream), reps, stream)
+                    tf = flops / (ms * 1e-3) / 1e12
+                    print(json.dumps({"sweep": name, "part": "key_tile", "key_tile": key_tile, "mode": mode,
+                                      "workload": workload_desc(wl), "attention_ms": ms, "attention_tflops": tf,
+                                      "frac_of_bf16_peak": tf / float(peaks["bf16_tflops"])}), flush=True)
+        del q, k, v, out, lse, bound, elig
+        torch.cuda.empty_cache()
+
+
+def sweep_masked(args, dev):
+    import torch
+
+    import frame_aligned_block_fsa_b300 as fsa
+    from frame_aligned_block_fsa_b300.inputs import make_workload_inputs
+    from frame_aligned_block_fsa_b300.workloads import WORKLOADS
+
+    stream = torch.cuda.current_stream()
+    peaks, _ = load_peaks()
+    reps = max(3, min(args.steps, 20))
+    for name in ("sr28k", "sr57k", "stress"):
+        wl = WORKLOADS[name]
+        q, k, v = (t.to(dev) for t in make_workload_inputs(wl))
+        H, N, D = wl.H, wl.N, wl.D
+        out = torch.empty((H, N, D), dtype=torch.float32, device=dev)
+        lse = torch.empty((H, N), dtype=torch.float32, device=dev)
+        bound = torch.empty((H, N), dtype=torch.float32, device=dev)
+        elig = torch.empty(H, dtype=torch.uint8, device=dev)
+        with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
+            active_pairs = plan.nnz() * wl.block * wl.block * H
+            flops = 4 * active_pairs * D
+            norms_ms = _timed(lambda: fsa.norms(q, k, plan, None, None, bound, elig, stream=stream), reps, stream)
+            base = {}
+            for mode in ("norm_bound", "online_max"):
+                base[mode] = _timed(lambda: fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound,
+                                                           eligible=elig, stream=stream), reps, stream)
+            for block in (128, 256, 512):
+                st = fsa.new_stats(dev)
+                fsa.forward_masked(q, k, v, plan, block=block, out=out, lse=lse, stats=st)
+                torch.cuda.synchronize()
+                stats = fsa.read_stats(st)
+                ms = _timed(lambda: fsa.forward_masked(q, k, v, plan, block=block, out=out, lse=lse, stream=stream),
+                            reps, stream)
+                tf = flops / (ms * 1e-3) / 1e12
+                print(json.dumps({
+                    "sweep": name, "part": "masked", "block": block, "workload": workload_desc(wl),
+                    "masked_ms": ms, "masked_tflops_active": tf, "frac_of_bf16_peak": tf / float(peaks["bf16_tflops"]),
+                    "computed_pairs_over_active": stats["pairs_visited"] / active_pairs,
+                    "frame_aligned_online_ms": base["online_max"], "frame_aligned_norm_bound_ms": base["norm_bound"],
+                    "norms_ms": norms_ms,
+                    # masked time over frame-aligned time (> 1: the frame-aligned layout is faster)
+                    "speedup_frame_aligned_online": ms / base["online_max"],
+                    "speedup_frame_aligned_norm_bound_incl_norms": ms / (base["norm_bound"] + norms_ms),
+                    "error": stats["error"]}), flush=True)
+        del q, k, v, out, lse, bound, elig
+        torch.cuda.empty_cache()
+
+
+def sweep_workloads(args, dev):
+    import torch
+
+    import frame_aligned_block_fsa_b300 as fsa
+    from frame_aligned_block_fsa_b300.inputs import make_workload_inputs
+    from frame_aligned_block_fsa_b300.workloads import WORKLOADS
+
     stream = torch.cuda.current_stream()
     peaks, _ = load_peaks()
     cached = {}  # the current workload's device inputs, shared by its two centring settings
@@ -284,16 +401,7 @@ def sweep(args):
         reps = max(3, min(args.steps, 20))
 
         def timed(fn):
-            for _ in range(3):
-                fn()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            a.record(stream)
-            for _ in range(reps):
-                fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            return a.elapsed_time(b) / reps
+            return _timed(fn, reps, stream)
 
         norms_ms = timed(lambda: fsa.norms(q, k, plan, None, None, bound, elig, stream=stream))
         # the row max comes from a running-max pass over every head
