@@ -273,7 +273,7 @@ def sweep(args):
     """One JSON line per measurement (not the bench contract line):
     workloads -- every workload in both softmax modes, and in norm_bound mode once more with
                  mean-centred keys;
-    key_tile  -- the attention kernel at key tiles of 16, 32, 48 and 64 keys, both modes, at the
+    key_tile  -- the attention kernel at key tiles of 16, 32, 48, 64, 96 and 128 keys, both modes, at the
                  28.8k and 57.6k workloads (the block geometry retuned for the softmax);
     masked    -- the masked-block comparison variant at blocks of 128, 256 and 512 tokens beside
                  the frame-aligned kernel in both modes, at the 28.8k, 57.6k and stress workloads."""
@@ -310,7 +310,7 @@ def sweep_key_tile(args, dev):
         with fsa.Plan(wl.F, wl.T, wl.w, wl.ref, wl.block) as plan:
             flops = plan.nnz() * 4 * wl.block * wl.block * D * H
             fsa.norms(q, k, plan, None, None, bound, elig, stream=stream)
-            for key_tile in (16, 32, 48, 64):
+            for key_tile in (16, 32, 48, 64, 96, 128):
                 plan.set_key_tile(key_tile)
                 for mode in ("norm_bound", "online_max"):
                     ms = _timed(lambda: fsa.forward_ex(q, k, v, plan, mode, out=out, lse=lse, bound=bound,

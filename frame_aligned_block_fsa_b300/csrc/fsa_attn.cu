@@ -15,16 +15,15 @@
 // (head, frame, 128-row query tile); CTA b takes items b, b + G, b + 2G, ... (G CTAs), in
 // head-major, frame-major order, so the CTAs that run at the same time share their heads'
 // K and V in L2.  Every role walks the same item sequence and, per item, the frame's key runs
-// in key tiles of at most NK (<= 64) keys (the last tile of a run may be narrower, a multiple
+// in key tiles of at most NK (<= 128) keys (the last tile of a run may be narrower, a multiple
 // of 16).  A tile counter g runs over all items of the CTA.
 //
 //   warps 0-11  softmax and epilogue, in three groups of four (warps 0-3, 4-7, 8-11), one warp
-//               per TMEM lane quarter: a thread owns one query row and all keys of its group's
-//               tiles.  On norm-bound items the groups take the tiles in turn (tile t of an item
-//               goes to group t % 3), so three tiles are in the softmax at once: with a fixed bound no
-//               tile waits for the one before it.  Running-max items go to group 0 alone (each
-//               tile needs the previous tile's max), whose threads then keep the row max without
-//               any exchange.
+//               per TMEM lane quarter: a thread owns one query row.  Every group takes every
+//               tile, its 16-key chunks c = group, group + 3, group + 6, so the twelve warps
+//               turn one tile into P together.  On norm-bound items each thread keeps a part of
+//               its row sum; on running-max items the groups also exchange their tile maxima
+//               through shared memory.
 //   warp 12     issues the S side (the warp runs the loop, one elected lane issues):
 //                 Q(item)  -> TMEM by tcgen05.cp from shared memory (two Q slots, so the copy
 //                             for the next item never touches the one in use)
@@ -34,21 +33,23 @@
 //               (the pipe takes an MMA only when it has room, so an issuing thread is held for
 //               about as long as its MMAs run; with two issuers one does its bookkeeping while
 //               the other feeds the pipe)
-//   warps 14-15 TMA producers, one for Q and K, one for V: K(g) and V(g) go to slot g & 3 of a K
-//               and a V ring (the slots of S buffer g & 3), each item's Q tile into its own
+//   warps 14-15 TMA producers, one for Q and K, one for V: K(g) and V(g) go to slot g & 1 of a K
+//               and a V ring (the slots of S buffer g & 1), each item's Q tile into its own
 //               staging buffer.
 //
-// Tensor work: S has four TMEM buffers (tile g uses buffer g & 3), so while the softmax turns
-// S(g) into P(g) the pipe has the three following S tiles and three PV products to compute.
-// PV(g) is issued once P(g) is in TMEM; S(g + 4) goes into the same buffer once PV(g) is done
-// (a commit of the PV issuer frees the buffer).
+// Tensor work: S has two TMEM buffers of 128 keys (tile g uses buffer g & 1), so while the
+// softmax turns S(g) into P(g) the pipe computes S(g + 1) and PV(g - 1).  PV(g) is issued once
+// P(g) is in TMEM; S(g + 2) goes into the same buffer once PV(g) is done (a commit of the PV
+// issuer frees the buffer).  A 128-key tile carries 1024 cycles of tensor work, twice a 64-key
+// one, against the same per-tile bookkeeping of the issuers (measured: 128-key tiles are the
+// fastest in both modes).
 //
 // One O accumulator: the epilogue of item k (O / l -> out) runs in all twelve softmax warps
-// when the tile walk reaches item k + 1 (the group that owns item k + 1's first tile first
-// produces its P), while the pipe computes S of item k + 1; the first PV of item k + 1 waits
-// until the epilogue has read O out of TMEM.
+// when the tile walk reaches item k + 1 (after they produced the P of its first tile), while
+// the pipe computes S of item k + 1; the first PV of item k + 1 waits until the epilogue has
+// read O out of TMEM.
 //
-// TMEM (512 columns): [Q slot 0: D/2][Q slot 1: D/2][S buffers 0-3: 64 each][O: D].
+// TMEM (512 columns): [Q slot 0: D/2][Q slot 1: D/2][S buffers 0-1: 128 each][O: D].
 // P(g) overwrites S(g) in its buffer after the softmax has read it: the 8 bf16-pair columns of
 // the 16 keys of chunk c go to the first 8 columns of that chunk, so each warp overwrites only
 // columns it has read itself.
@@ -67,8 +68,9 @@ constexpr int kGroupWarps = 4;              // one warp per lane quarter
 constexpr int kSoftWarps = kGroups * kGroupWarps;  // 12
 constexpr int kAttnThreads = 32 * (kSoftWarps + 4);  // + two tcgen05 issuers and two TMA warps
 constexpr int kWarpS = kSoftWarps, kWarpPV = kSoftWarps + 1, kWarpTmaK = kSoftWarps + 2, kWarpTmaV = kSoftWarps + 3;
-constexpr int kNBuf = 4;                    // S buffers
-constexpr int kBufCols = 64;                // TMEM columns (= keys) of an S buffer
+constexpr int kNBuf = 2;                    // S buffers
+constexpr int kBufShift = 1;                // log2(kNBuf): tile g uses buffer g & (kNBuf - 1), phase g >> kBufShift
+constexpr int kBufCols = 128;               // TMEM columns (= keys) of an S buffer
 // Frames whose key runs are copied to shared memory when the kernel starts; larger plans
 // read them from global memory.
 constexpr int kSmemRunFrames = 256;
@@ -77,12 +79,12 @@ template <int D>
 struct AttnCfg {
     static_assert(D == 64 || D == 128, "head dim");
     static constexpr int PANELS = D / 64;              // 64-element (128 B) swizzle panels of a row
-    static constexpr int KV_PANEL = kBufCols * 128;    // 64 rows x 128 B
-    static constexpr int SLOT_BYTES = PANELS * KV_PANEL;  // one K or V tile of up to 64 rows
+    static constexpr int KV_PANEL = kBufCols * 128;    // 128 rows x 128 B
+    static constexpr int SLOT_BYTES = PANELS * KV_PANEL;  // one K or V tile of up to 128 rows
     static constexpr int Q_PANEL = 128 * 128;          // 128 rows x 128 B
     static constexpr int Q_BYTES = PANELS * Q_PANEL;
-    // K(g) and V(g) go to slot g & 3 of a K and a V ring, the slots of S buffer g & 3: the
-    // commit that ends S(g) frees K slot g & 3, the one that ends PV(g) frees V slot g & 3.
+    // K(g) and V(g) go to slot g & 1 of a K and a V ring, the slots of S buffer g & 1: the
+    // commit that ends S(g) frees K slot g & 1, the one that ends PV(g) frees V slot g & 1.
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_BYTES;
     static constexpr int V_OFF = K_OFF + kNBuf * SLOT_BYTES;
@@ -93,8 +95,7 @@ struct AttnCfg {
     static constexpr int B_QFULL = 2 * kNBuf;          // the staged Q tile landed
     static constexpr int B_QEMPTY = B_QFULL + 1;       // its copy into TMEM is done
     static constexpr int B_SFULL = B_QEMPTY + 1;       // kNBuf: S in buffer b complete (K slot b free)
-    // kNBuf: P in buffer b written: kSoftWarps arrivals, 3 from each warp of the owning group
-    // on norm-bound tiles, 1 from every softmax warp on running-max tiles
+    // kNBuf: P in buffer b written: kSoftWarps arrivals, one from every softmax warp
     static constexpr int B_PFULL = B_SFULL + kNBuf;
     static constexpr int B_OFULL = B_PFULL + kNBuf;    // the last PV of an item done: O final
     static constexpr int B_OFREE = B_OFULL + 1;        // the epilogue has read O (all softmax warps)
@@ -355,7 +356,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     ++nq;
                 }
                 const int b = n & (kNBuf - 1);
-                if (n >= kNBuf && !wt.bar(p, bar(b_free + b), ((n >> 2) & 1) ^ 1, SITE_PROD_EMPTY)) break;
+                if (n >= kNBuf && !wt.bar(p, bar(b_free + b), ((n >> kBufShift) & 1) ^ 1, SITE_PROD_EMPTY)) break;
                 mbar_arrive_expect_tx(bar(b_full + b), kv_bytes);
                 for (int pn = 0; pn < C::PANELS; ++pn)
                     tma_load_2d_hint(ring + b * C::SLOT_BYTES + pn * C::KV_PANEL, map, pn * 64, hrow + start,
@@ -365,7 +366,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // Every copy this thread issued must land before the CTA may exit.
             if (nq > 0) wt.bar(p, bar(C::B_QFULL), (nq - 1) & 1, SITE_DRAIN, false);
             for (int u = n > kNBuf ? n - kNBuf : 0; u < n; ++u)
-                wt.bar(p, bar(b_full + (u & (kNBuf - 1))), (u >> 2) & 1, SITE_DRAIN, false);
+                wt.bar(p, bar(b_full + (u & (kNBuf - 1))), (u >> kBufShift) & 1, SITE_DRAIN, false);
         }
     } else if (warp == kWarpS) {
         // ------------------------------------------------------------- tcgen05 issuer: Q, S
@@ -406,10 +407,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // S(x) overwrites the buffer of tile x - 4, whose PV must be done; K(x) must be in
             if (!__all_sync(0xffffffffu, b_seen) &&
                 !(ok = __all_sync(0xffffffffu,
-                                  wt.bar(p, bar(C::B_BFREE + buf), ((x >> 2) & 1) ^ 1, SITE_MMA_P))))
+                                  wt.bar(p, bar(C::B_BFREE + buf), ((x >> kBufShift) & 1) ^ 1, SITE_MMA_P))))
                 break;
             if (!__all_sync(0xffffffffu, k_seen) &&
-                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_KFULL + buf), (x >> 2) & 1, SITE_MMA_SLOT))))
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_KFULL + buf), (x >> kBufShift) & 1, SITE_MMA_SLOT))))
                 break;
             tc_fence_after();
             const uint64_t b0 = smem_desc_sw128(kslot(buf), 16, 1024);
@@ -418,8 +419,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (leader) mma_ts(tbase + C::t_s(buf), tq, b0, idesc, 0u);
             {
                 const int xn = x + 1, bn = xn & (kNBuf - 1);
-                k_seen = mbar_test_wait(bar(C::B_KFULL + bn), (xn >> 2) & 1);
-                b_seen = xn < kNBuf || mbar_test_wait(bar(C::B_BFREE + bn), ((xn >> 2) & 1) ^ 1);
+                k_seen = mbar_test_wait(bar(C::B_KFULL + bn), (xn >> kBufShift) & 1);
+                b_seen = xn < kNBuf || mbar_test_wait(bar(C::B_BFREE + bn), ((xn >> kBufShift) & 1) ^ 1);
             }
             if (leader) {
 #pragma unroll
@@ -459,10 +460,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     break;
             }
             if (!__all_sync(0xffffffffu, v_seen) &&
-                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_VFULL + buf), (g >> 2) & 1, SITE_MMA_SLOT))))
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_VFULL + buf), (g >> kBufShift) & 1, SITE_MMA_SLOT))))
                 break;
             if (!__all_sync(0xffffffffu, p_seen) &&
-                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_PFULL + buf), (g >> 2) & 1, SITE_MMA_P))))
+                !(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_PFULL + buf), (g >> kBufShift) & 1, SITE_MMA_P))))
                 break;
             tc_fence_after();
             // O += P(g) V(g): A = P from the S buffer (16 keys = 8 columns per step)
@@ -471,8 +472,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mma_ts(tbase + C::T_O, tbase + C::t_s(buf), b0, C::IDESC_O, t_first ? 0u : 1u);
             {
                 const int gn = g + 1, bn = gn & (kNBuf - 1);
-                p_seen = mbar_test_wait(bar(C::B_PFULL + bn), (gn >> 2) & 1);
-                v_seen = mbar_test_wait(bar(C::B_VFULL + bn), (gn >> 2) & 1);
+                p_seen = mbar_test_wait(bar(C::B_PFULL + bn), (gn >> kBufShift) & 1);
+                v_seen = mbar_test_wait(bar(C::B_VFULL + bn), (gn >> kBufShift) & 1);
             }
             if (leader) {
 #pragma unroll
@@ -603,8 +604,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             return true;
         };
 
-        // Walk the items; per item, this group's tiles: every third tile on norm-bound items
-        // (tile t of an item goes to group t % 3), all tiles for group 0 on running-max items.
+        // Walk the items; per item, every tile, this group's chunks of each.
         int g0 = 0;  // CTA tile index of the item's first tile
         for (int item = blockIdx.x, local = 0; ok && item < p.total; item += gridDim.x, ++local) {
             const int h = item / p.per_head;
@@ -657,18 +657,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l = 0.0f;
             if (p.stats && p.mode == 0 && !use_bound && warp == 0 && lane == 0 && loc == 0)
                 atomicAdd(&p.stats->fallback_heads, 1);
-            // Norm-bound items: tile t goes to group t % 3 (the split of the row sum over the groups,
-            // and so its rounding, depends on the item alone).  Running-max items: every group takes
-            // every tile, each its own 16-key chunks (chunk c to group c % 3).  One loop per kind,
-            // so each stays small.
+            // Every group takes every tile: its 16-key chunks c = group, group + 3, group + 6 (the
+            // split of the row sum over the groups, and so its rounding, depends on the tile
+            // alone).  One loop per kind of item, so each stays small.
             if (use_bound) {
-                // a group that does not take the item's first tile finishes the previous item
-                // now; the one that does, right after producing that tile's P
-                if (group != 0 && pv_flags >= 0) {
-                    if (!(ok = epilogue())) break;
-                    pv_flags = -1;
-                }
-                for (int t = group; t < n; t += kGroups) {
+                const float nb2 = -b_nat * kLog2e;
+                for (int t = 0; t < n; ++t) {
                     const int g = g0 + t;
                     const int width = t == n0 - 1 ? w0 : (t == n - 1 ? w1 : p.NK);
                     const int nch = width / 16;
@@ -676,58 +670,57 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint32_t tS = tbase + lane_off + C::t_s(buf);
                     const float c2 = row < (flags & 0xff) ? p.scale_log2 : 0.0f;
                     // the vote keeps the warp converged for the warp-collective TMEM accesses
-                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
+                    if (!(ok = __all_sync(0xffffffffu,
+                                          wt.bar(p, bar(C::B_SFULL + buf), (g >> kBufShift) & 1, SITE_SOFT_S))))
                         break;
                     tc_fence_after();
-                    // p = 2^(s c2 - b log2 e) over the whole tile, read in halves of up to 32 keys
-                    // (chunks 2hh, 2hh + 1), one loop body for both, so the hot code stays small;
-                    // packed to bf16 over the S columns just read; four partial sums of the fp32
-                    // weights (short add chains)
-                    const float nb2 = -b_nat * kLog2e;
-                    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+                    // p = 2^(s c2 - b log2 e) with the fixed bound, packed to bf16 over the first 8
+                    // columns of each chunk just read; four partial sums of the fp32 weights.  Two
+                    // passes (chunks group and group + 3, then group + 6) bound the live scores.
+                    const float2 c2x2 = make_float2(c2, c2), nb2x2 = make_float2(nb2, nb2);
+                    float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
 #pragma unroll 1
-                    for (int hh = 0; hh < 2; ++hh) {
-                        if (2 * hh >= nch) break;
-                        const bool two = 2 * hh + 1 < nch;
+                    for (int ph = 0; ph < 2; ++ph) {
+                        const int c0 = group + 6 * ph;  // first chunk of this pass
+                        const bool u0 = c0 < nch, u1 = ph == 0 && c0 + 3 < nch;
+                        if (!u0) break;
                         float s[32];
-                        uint32_t pk[16];
-                        tmem_ld_x16(tS + 32 * hh, s);
-                        if (two) tmem_ld_x16(tS + 32 * hh + 16, s + 16);
+                        tmem_ld_x16(tS + 16 * c0, s);
+                        if (u1) tmem_ld_x16(tS + 16 * (c0 + 3), s + 16);
                         tmem_ld_wait();
 #pragma unroll
                         for (int i = 0; i < 32; ++i) reg_fence(s[i]);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+                        for (int j = 0; j < 2; ++j) {
+                            if (j == 0 || u1) {
+                                float* sj = s + 16 * j;
+                                uint32_t pk[8];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+                                for (int i = 0; i < 16; i += 2) {
+                                    const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
+                                    sj[i] = ex2(e.x);
+                                    sj[i + 1] = ex2(e.y);
+                                }
 #pragma unroll
-                        for (int i = 0; i < 16; i += 4) {
-                            a0 += s[i];
-                            a1 += s[i + 1];
-                            a2 += s[i + 2];
-                            a3 += s[i + 3];
-                        }
-                        tmem_st_x8(tS + 32 * hh, pk);
-                        if (two) {
+                                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
 #pragma unroll
-                            for (int i = 16; i < 32; i += 4) {
-                                a0 += s[i];
-                                a1 += s[i + 1];
-                                a2 += s[i + 2];
-                                a3 += s[i + 3];
+                                for (int i = 0; i < 16; i += 4) {
+                                    a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
+                                    a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
+                                }
+                                tmem_st_x8(tS + 16 * (c0 + 3 * j), pk);
                             }
-                            tmem_st_x8(tS + 32 * hh + 16, pk + 8);
                         }
-                }
-                l += (a0 + a1) + (a2 + a3);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cnt(bar(C::B_PFULL + buf), 3);
-                if (pv_flags >= 0) {
-                    if (!(ok = epilogue())) break;
-                    pv_flags = -1;
-                }
+                    }
+                    l += (a01.x + a01.y) + (a23.x + a23.y);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
+                    if (pv_flags >= 0) {
+                        if (!(ok = epilogue())) break;
+                        pv_flags = -1;
+                    }
                 }
             } else {
                 for (int t = 0; t < n; ++t) {
@@ -739,124 +732,120 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // masked variant: rows past the sequence have an empty key interval instead
                     const float c2 = (MASKED || row < (flags & 0xff)) ? p.scale_log2 : 0.0f;
                     // the vote keeps the warp converged for the warp-collective TMEM accesses
-                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_SFULL + buf), (g >> 2) & 1, SITE_SOFT_S))))
+                    if (!(ok = __all_sync(0xffffffffu,
+                                          wt.bar(p, bar(C::B_SFULL + buf), (g >> kBufShift) & 1, SITE_SOFT_S))))
                         break;
                     tc_fence_after();
-                    // Running max, shared by all groups: this warp's chunks are c = group and
-                    // group + 3.  The groups exchange their tile maxima; the exponentials use a
-                    // reference m2 that moves only when the row max passes it by more than 8 (so
-                    // every p stays below 2^8), and only then is the row's accumulator rescaled.
-                    const bool has0 = group < nch, has1 = group + 3 < nch;
-                    float s[32];
-                    uint32_t pk[16];
-                    if (has0) tmem_ld_x16(tS + 16 * group, s);
-                    if (has1) tmem_ld_x16(tS + 16 * (group + 3), s + 16);
+                    // Running max, shared by all groups.  The groups exchange their tile maxima;
+                    // the exponentials use a reference m2 that moves only when the row max passes
+                    // it by more than 8 (so every p stays below 2^8), and only then is the row's
+                    // accumulator rescaled.
+                    const bool h0 = group < nch, h1 = group + 3 < nch, h2 = group + 6 < nch;
+                    float s[48];
+                    if (h0) tmem_ld_x16(tS + 16 * group, s);
+                    if (h1) tmem_ld_x16(tS + 16 * (group + 3), s + 16);
+                    if (h2) tmem_ld_x16(tS + 16 * (group + 6), s + 32);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) reg_fence(s[i]);
+                    for (int i = 0; i < 48; ++i) reg_fence(s[i]);
                     if constexpr (MASKED) {
                         // mask predicates, on tiles that are not wholly inside the row's interval
                         const int j0 = kst + t * p.NK;
                         if (!(j0 >= ja && j0 + width <= jb)) {
                             const unsigned span = static_cast<unsigned>(jb - ja);
-                            const int c0 = j0 + 16 * group - ja, c1 = j0 + 16 * (group + 3) - ja;
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                if (static_cast<unsigned>(c0 + e) >= span) s[e] = -INFINITY;
-                                if (static_cast<unsigned>(c1 + e) >= span) s[16 + e] = -INFINITY;
+                            for (int j = 0; j < 3; ++j) {
+                                const int cj = j0 + 16 * (group + 3 * j) - ja;
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    if (static_cast<unsigned>(cj + e) >= span) s[16 * j + e] = -INFINITY;
                             }
                         }
                     }
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-                    if (has0) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-                }
-                if (has1) {
+                    for (int j = 0; j < 3; ++j) {
+                        if (j == 0 ? h0 : (j == 1 ? h1 : h2)) {
 #pragma unroll
-                    for (int e = 16; e < 32; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[e]);
-                }
-                // exchange slots double-buffered by parity: a warp writes exchange n + 2's slot
-                // only after every partner has written n + 1's, i.e. after it read n's
-                const uint32_t mcount = sbase + C::MISC_OFF + 24u + 4u * quarter;
-                const uint32_t ms = sbase + C::MMAX_OFF + (n_mx & 1) * (kGroups * 128 * 4) + 4u * row;
-                st_shared_f32(ms + 512 * group, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
-                __syncwarp();
-                if (lane == 0) red_release_shared_add(mcount, 1u);
-                ++n_mx;
-                if (!(ok = __all_sync(0xffffffffu, wt.counter(p, mcount, kGroups * n_mx, SITE_SOFT_X)))) break;
-                float tmax = ld_shared_f32(ms);
-#pragma unroll
-                for (int j = 1; j < kGroups; ++j) tmax = fmaxf(tmax, ld_shared_f32(ms + 512 * j));
-                const float m_tile = tmax * c2;
-                mt = fmaxf(mt, m_tile);
-                float alpha = 1.0f;
-                if (t == 0) {
-                    m2 = m_tile;  // O and l start from zero: nothing to rescale
-                } else if (__any_sync(0xffffffffu, m_tile > m2 + 8.0f)) {
-                    // O may be rescaled only once PV of the item's previous tile is done
-                    if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_BFREE + ((g - 1) & (kNBuf - 1))),
-                                                              ((g - 1) >> 2) & 1, SITE_SOFT_O))))
-                        break;
-                    tc_fence_after();
-                    const float m_new = m_tile > m2 + 8.0f ? m_tile : m2;
-                    // (masked variant: a row with no key yet keeps m2 = -inf and alpha = 1)
-                    alpha = (!MASKED || m_new > m2) ? ex2(m2 - m_new) : 1.0f;
-                    m2 = m_new;
-                    // this warp's share of the row's accumulator (the epilogue's column split)
-                    constexpr int NCHO = D / 16;
-                    const int cb = group * NCHO / kGroups, ce = (group + 1) * NCHO / kGroups;
-                    const uint32_t tO = tbase + lane_off + C::T_O;
-#pragma unroll 1
-                    for (int c = cb; c < ce; ++c) {
-                        float o[16];
-                        tmem_ld_x16(tO + 16 * c, o);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            reg_fence(o[e]);
-                            o[e] *= alpha;
+                            for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[16 * j + e]);
                         }
-                        tmem_st_x16(tO + 16 * c, o);
                     }
-                }
-                // masked variant: m2 = -inf only while every key of the row so far, this tile's
-                // included, is masked; their weights are 2^-inf = 0
-                const float nb2 = (MASKED && m2 == -INFINITY) ? 0.0f : -m2;
-                float a0 = 0.0f, a1 = 0.0f;
-                if (has0) {
+                    // exchange slots double-buffered by parity: a warp writes exchange n + 2's slot
+                    // only after every partner has written n + 1's, i.e. after it read n's
+                    const uint32_t mcount = sbase + C::MISC_OFF + 24u + 4u * quarter;
+                    const uint32_t ms = sbase + C::MMAX_OFF + (n_mx & 1) * (kGroups * 128 * 4) + 4u * row;
+                    st_shared_f32(ms + 512 * group, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                    __syncwarp();
+                    if (lane == 0) red_release_shared_add(mcount, 1u);
+                    ++n_mx;
+                    if (!(ok = __all_sync(0xffffffffu, wt.counter(p, mcount, kGroups * n_mx, SITE_SOFT_X)))) break;
+                    float tmax = ld_shared_f32(ms);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+                    for (int j = 1; j < kGroups; ++j) tmax = fmaxf(tmax, ld_shared_f32(ms + 512 * j));
+                    const float m_tile = tmax * c2;
+                    mt = fmaxf(mt, m_tile);
+                    float alpha = 1.0f;
+                    if (t == 0) {
+                        m2 = m_tile;  // O and l start from zero: nothing to rescale
+                    } else if (__any_sync(0xffffffffu, m_tile > m2 + 8.0f)) {
+                        // O may be rescaled only once PV of the item's previous tile is done
+                        if (!(ok = __all_sync(0xffffffffu, wt.bar(p, bar(C::B_BFREE + ((g - 1) & (kNBuf - 1))),
+                                                                  ((g - 1) >> kBufShift) & 1, SITE_SOFT_O))))
+                            break;
+                        tc_fence_after();
+                        const float m_new = m_tile > m2 + 8.0f ? m_tile : m2;
+                        // (masked variant: a row with no key yet keeps m2 = -inf and alpha = 1)
+                        alpha = (!MASKED || m_new > m2) ? ex2(m2 - m_new) : 1.0f;
+                        m2 = m_new;
+                        // this warp's share of the row's accumulator (the epilogue's column split)
+                        constexpr int NCHO = D / 16;
+                        const int cb = group * NCHO / kGroups, ce = (group + 1) * NCHO / kGroups;
+                        const uint32_t tO = tbase + lane_off + C::T_O;
+#pragma unroll 1
+                        for (int c = cb; c < ce; ++c) {
+                            float o[16];
+                            tmem_ld_x16(tO + 16 * c, o);
+                            tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        a0 += s[i];
-                        a1 += s[i + 1];
+                            for (int e = 0; e < 16; ++e) {
+                                reg_fence(o[e]);
+                                o[e] *= alpha;
+                            }
+                            tmem_st_x16(tO + 16 * c, o);
+                        }
                     }
-                    tmem_st_x8(tS + 16 * group, pk);
-                }
-                if (has1) {
+                    // masked variant: m2 = -inf only while every key of the row so far, this tile's
+                    // included, is masked; their weights are 2^-inf = 0
+                    const float nb2 = (MASKED && m2 == -INFINITY) ? 0.0f : -m2;
+                    const float2 c2x2 = make_float2(c2, c2), nb2x2 = make_float2(nb2, nb2);
+                    float2 a01 = make_float2(0.0f, 0.0f);  // two partial sums in one packed add
 #pragma unroll
-                    for (int i = 16; i < 32; ++i) s[i] = ex2(fmaf(s[i], c2, nb2));
+                    for (int j = 0; j < 3; ++j) {
+                        if (j == 0 ? h0 : (j == 1 ? h1 : h2)) {
+                            float* sj = s + 16 * j;
+                            uint32_t pk[8];
 #pragma unroll
-                    for (int i = 8; i < 16; ++i) pk[i] = pack_bf16x2(s[2 * i], s[2 * i + 1]);
+                            for (int i = 0; i < 16; i += 2) {
+                                const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
+                                sj[i] = ex2(e.x);
+                                sj[i + 1] = ex2(e.y);
+                            }
 #pragma unroll
-                    for (int i = 16; i < 32; i += 2) {
-                        a0 += s[i];
-                        a1 += s[i + 1];
+                            for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
+#pragma unroll
+                            for (int i = 0; i < 16; i += 2) a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
+                            tmem_st_x8(tS + 16 * (group + 3 * j), pk);
+                        }
                     }
-                    tmem_st_x8(tS + 16 * (group + 3), pk + 8);
-                }
-                l = l * alpha + (a0 + a1);
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
-                if (pv_flags >= 0) {
-                    if (!(ok = epilogue())) break;
-                    pv_flags = -1;
-                }
+                    l = l * alpha + (a01.x + a01.y);
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
+                    if (pv_flags >= 0) {
+                        if (!(ok = epilogue())) break;
+                        pv_flags = -1;
+                    }
                 }
             }
             if (!ok) break;

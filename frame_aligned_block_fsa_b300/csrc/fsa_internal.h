@@ -15,8 +15,8 @@ namespace fsa {
 constexpr int kMaxRuns = 2;
 constexpr int kRunStride = 1 + 2 * kMaxRuns;
 
-// Largest key tile of the attention kernel (its four S buffers hold 64 columns each).
-constexpr int kMaxKeyTile = 64;
+// Largest key tile of the attention kernel (its two S buffers hold 128 columns each).
+constexpr int kMaxKeyTile = 128;
 
 // Work item of the masked block variant (one 128-row query tile of a query block on the padded
 // sequence): [first query token, first key token, keys (a multiple of the block size), 0, 0].

@@ -109,14 +109,13 @@ int fsa_plan_export(fsa_plan_t plan, int32_t* row_ptr, int32_t* col_idx, int64_t
 int fsa_plan_set_tau(fsa_plan_t plan, float tau);
 
 /*
- * fsa_plan_set_key_tile -- keys per tensor-core tile: 0 = automatic (64, the kernel's
- * largest), else a multiple of 16 in [16, 128].  Every key run (a whole number of frames) is
- * cut into tiles of this many keys and one last narrower tile of the rest (a multiple of 16,
- * since T is); no tile is partially masked.  Results are bitwise independent of `block`;
- * they may change in the last bits with the key tile (summation order).
- * Errors: FSA_ERR_INVALID_ARG for a NULL plan or a key tile outside that set; a tile above
- * the attention kernel's limit (64 keys, the width of its S buffers in TMEM) makes
- * fsa_forward* return FSA_ERR_UNSUPPORTED before any device work.
+ * fsa_plan_set_key_tile -- keys per tensor-core tile: 0 = automatic (128, the kernel's
+ * largest, the width of its S buffers in TMEM, and the fastest measured), else a multiple of
+ * 16 in [16, 128].  Every key run (a whole number of frames) is cut into tiles of this many
+ * keys and one last narrower tile of the rest (a multiple of 16, since T is); no tile is
+ * partially masked.  Results are bitwise independent of `block`; they may change in the last
+ * bits with the key tile (summation order).
+ * Errors: FSA_ERR_INVALID_ARG for a NULL plan or a key tile outside that set.
  */
 int fsa_plan_set_key_tile(fsa_plan_t plan, int key_tile);
 
@@ -226,7 +225,7 @@ int fsa_forward_host(const uint16_t* q, const uint16_t* k, const uint16_t* v, fl
  *     through their log-sum-exps; pass 1 writes its fp32 partial out and lse to plan-owned
  *     buffers (H*N*D + H*N floats, grown on first use).
  * Both passes run the running-max softmax (the pages' comparison state has no norm bound), on
- * the same persistent tcgen05 kernel as fsa_forward (128-row query tiles, 64-key tiles).  The
+ * the same persistent tcgen05 kernel as fsa_forward (128-row query tiles, 128-key tiles).  The
  * result is the attention fsa_forward computes, up to rounding.
  *   q, k, v, out, lse, H, D, stream: as fsa_forward.  plan: its F, T, w and ref are used (its
  *   block size is not).  block: a multiple of 128 from 128 to 1024.  dev_stats: optional, as in

@@ -153,12 +153,6 @@ def test_forward_rejects_bad_arguments_before_device_work(lib):
         assert fh(*hargs(out=None)) == fsa.FSA_ERR_INVALID_ARG
         assert fh(*hargs(plan=None)) == fsa.FSA_ERR_INVALID_ARG
         assert fh(*hargs(H=0)) == fsa.FSA_OK
-    # a key tile above the kernel's S-buffer width (64 keys) is refused before device work
-    with fsa.Plan(4, 256, 1, 0, 64) as p:
-        p.set_key_tile(128)
-        assert lib.fsa_forward(fake, fake, fake, fake, fake, 2, 128, p.handle, 0, None) == fsa.FSA_ERR_UNSUPPORTED
-        assert lib.fsa_forward_host(fake, fake, fake, fake, fake, 2, 128, p.handle, 0, 0, None) == \
-            fsa.FSA_ERR_UNSUPPORTED
     # H * N beyond int32 row indexing
     with fsa.Plan(16, 3600, 1, 0, 144) as p:
         assert lib.fsa_forward(fake, fake, fake, fake, fake, 40000, 128, p.handle, 0, None) == \

@@ -445,9 +445,10 @@ def test_edge_shapes_full_parity(dev, oracle_mod, shape, mode):
     _check(res["out"], res["lse"], ref_res["out"], ref_res["lse"])
 
 
-@pytest.mark.parametrize("key_tile", [16, 32, 48, 64])
+@pytest.mark.parametrize("key_tile", [16, 32, 48, 64, 112, 128])
 def test_key_tile_override(dev, oracle_mod, key_tile):
-    # T = 1200: 32 and 64 leave a narrower last tile in every key run (16 and 48 keys)
+    # T = 1200: 32, 64, 112 and 128 leave a narrower last tile in every key run (16, 48, 80 and
+    # 48 keys)
     H, F, T, D, w, ref, block = 2, 5, 1200, 128, 2, 0, 80
     q, k, v = make_qkv(H, F * T, D, seed=99)
     heads = np.repeat(np.arange(H, dtype=np.int32), 64)
