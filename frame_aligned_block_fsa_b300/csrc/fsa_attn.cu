@@ -71,6 +71,10 @@ constexpr int kWarpS = kSoftWarps, kWarpPV = kSoftWarps + 1, kWarpTmaK = kSoftWa
 constexpr int kNBuf = 2;                    // S buffers
 constexpr int kBufShift = 1;                // log2(kNBuf): tile g uses buffer g & (kNBuf - 1), phase g >> kBufShift
 constexpr int kBufCols = 128;               // TMEM columns (= keys) of an S buffer
+// The softmax turns a tile into P in two passes: chunks group and group + 3 of every group (the
+// first kPassChunks 16-key chunks), then chunk group + 6; the PV MMAs of the first pass's keys
+// start while the second pass runs.
+constexpr int kPassChunks = 2 * 3;
 // Frames whose key runs are copied to shared memory when the kernel starts; larger plans
 // read them from global memory.
 constexpr int kSmemRunFrames = 256;
@@ -95,9 +99,12 @@ struct AttnCfg {
     static constexpr int B_QFULL = 2 * kNBuf;          // the staged Q tile landed
     static constexpr int B_QEMPTY = B_QFULL + 1;       // its copy into TMEM is done
     static constexpr int B_SFULL = B_QEMPTY + 1;       // kNBuf: S in buffer b complete (K slot b free)
-    // kNBuf: P in buffer b written: kSoftWarps arrivals, one from every softmax warp
+    // kNBuf: P of chunks 0-5 in buffer b written (the softmax's first pass: chunks group and
+    // group + 3 of every group): kSoftWarps arrivals, one from every softmax warp
     static constexpr int B_PFULL = B_SFULL + kNBuf;
-    static constexpr int B_OFULL = B_PFULL + kNBuf;    // the last PV of an item done: O final
+    // kNBuf: P of chunks 6-7 written (the second pass: chunk group + 6), kSoftWarps arrivals
+    static constexpr int B_PFULL2 = B_PFULL + kNBuf;
+    static constexpr int B_OFULL = B_PFULL2 + kNBuf;   // the last PV of an item done: O final
     static constexpr int B_OFREE = B_OFULL + 1;        // the epilogue has read O (all softmax warps)
     static constexpr int B_BFREE = B_OFREE + 1;        // kNBuf: PV of buffer b's tile done (S buffer b and V
                                                        // slot b free)
@@ -296,6 +303,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int b = 0; b < kNBuf; ++b) {
             mbar_init(bar(C::B_SFULL + b), 1);
             mbar_init(bar(C::B_PFULL + b), kSoftWarps);
+            mbar_init(bar(C::B_PFULL2 + b), kSoftWarps);
         }
         mbar_init(bar(C::B_OFULL), 1);
         mbar_init(bar(C::B_OFREE), kSoftWarps);
@@ -477,7 +485,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (leader) {
 #pragma unroll
-                for (int ks = 1; ks < kBufCols / 16; ++ks)
+                for (int ks = 1; ks < kPassChunks; ++ks)
+                    if (ks < t_width / 16)
+                        mma_ts(tbase + C::T_O, tbase + C::t_s(buf) + ks * 16,
+                               b0 + static_cast<uint64_t>((ks * 16 * 128) >> 4), C::IDESC_O, 1u);
+            }
+            __syncwarp();
+            // the last two chunks of P come from the softmax's second pass (every tile's phase of
+            // that barrier is waited for, so this thread never falls two phases behind)
+            if (!(ok = __all_sync(0xffffffffu,
+                                  wt.bar(p, bar(C::B_PFULL2 + buf), (g >> kBufShift) & 1, SITE_MMA_P))))
+                break;
+            tc_fence_after();
+            if (leader) {
+#pragma unroll
+                for (int ks = kPassChunks; ks < kBufCols / 16; ++ks)
                     if (ks < t_width / 16)
                         mma_ts(tbase + C::T_O, tbase + C::t_s(buf) + ks * 16,
                                b0 + static_cast<uint64_t>((ks * 16 * 128) >> 4), C::IDESC_O, 1u);
@@ -683,40 +705,42 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int ph = 0; ph < 2; ++ph) {
                         const int c0 = group + 6 * ph;  // first chunk of this pass
                         const bool u0 = c0 < nch, u1 = ph == 0 && c0 + 3 < nch;
-                        if (!u0) break;
-                        float s[32];
-                        tmem_ld_x16(tS + 16 * c0, s);
-                        if (u1) tmem_ld_x16(tS + 16 * (c0 + 3), s + 16);
-                        tmem_ld_wait();
+                        if (u0) {
+                            float s[32];
+                            tmem_ld_x16(tS + 16 * c0, s);
+                            if (u1) tmem_ld_x16(tS + 16 * (c0 + 3), s + 16);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) reg_fence(s[i]);
+                            for (int i = 0; i < 32; ++i) reg_fence(s[i]);
 #pragma unroll
-                        for (int j = 0; j < 2; ++j) {
-                            if (j == 0 || u1) {
-                                float* sj = s + 16 * j;
-                                uint32_t pk[8];
+                            for (int j = 0; j < 2; ++j) {
+                                if (j == 0 || u1) {
+                                    float* sj = s + 16 * j;
+                                    uint32_t pk[8];
 #pragma unroll
-                                for (int i = 0; i < 16; i += 2) {
-                                    const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
-                                    sj[i] = ex2(e.x);
-                                    sj[i + 1] = ex2(e.y);
+                                    for (int i = 0; i < 16; i += 2) {
+                                        const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
+                                        sj[i] = ex2(e.x);
+                                        sj[i + 1] = ex2(e.y);
+                                    }
+#pragma unroll
+                                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
+#pragma unroll
+                                    for (int i = 0; i < 16; i += 4) {
+                                        a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
+                                        a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
+                                    }
+                                    tmem_st_x8(tS + 16 * (c0 + 3 * j), pk);
                                 }
-#pragma unroll
-                                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
-#pragma unroll
-                                for (int i = 0; i < 16; i += 4) {
-                                    a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
-                                    a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
-                                }
-                                tmem_st_x8(tS + 16 * (c0 + 3 * j), pk);
                             }
                         }
+                        // this pass's P is in TMEM: the PV MMAs of its chunks may start
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar((ph == 0 ? C::B_PFULL : C::B_PFULL2) + buf));
                     }
                     l += (a01.x + a01.y) + (a23.x + a23.y);
-                    tmem_st_wait();
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
                     if (pv_flags >= 0) {
                         if (!(ok = epilogue())) break;
                         pv_flags = -1;
@@ -836,12 +860,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             for (int i = 0; i < 16; i += 2) a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
                             tmem_st_x8(tS + 16 * (group + 3 * j), pk);
                         }
+                        if (j == 1) {
+                            // chunks group and group + 3 are in TMEM: the first pass is done
+                            tmem_st_wait();
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
+                        }
                     }
                     l = l * alpha + (a01.x + a01.y);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(bar(C::B_PFULL + buf));
+                    if (lane == 0) mbar_arrive(bar(C::B_PFULL2 + buf));
                     if (pv_flags >= 0) {
                         if (!(ok = epilogue())) break;
                         pv_flags = -1;
