@@ -638,9 +638,9 @@ def main():
                            "frac": norms_bytes / (norms_avg * 1e-3) / 1e9 / float(peaks["hbm_gbs"]),
                            "ms_avg": norms_avg, "algorithmic_bytes": norms_bytes},
         "clocks": clk,
-        # per step: 3 norm kernels (4 with centred keys), or the prep's 6 (rms, K/V projection,
+        # per step: 2 norm kernels (3 with centred keys), or the prep's 6 (rms, K/V projection,
         # frame key sums, key-set statistics, Q projection, eligibility), + the attention kernel
-        "gpu_launches": (7 if args.prep else (5 if args.center_keys else 4)) * args.steps,
+        "gpu_launches": (7 if args.prep else (4 if args.center_keys else 3)) * args.steps,
         "e2e": e2e,
     }
     sus = extras.pop("sustained", None)

@@ -172,7 +172,7 @@ int ensure_workspace(fsa_plan_s* P, int H, int D)
     if ((rc = grow(&P->d_pmax, &P->cap_pmax, hf * chunks)) != FSA_OK) return rc;
     const int64_t had = P->cap_tickets, had_h = P->cap_htickets;
     if ((rc = grow(&P->d_tickets, &P->cap_tickets, hf)) != FSA_OK) return rc;
-    if ((rc = grow(&P->d_htickets, &P->cap_htickets, static_cast<int64_t>(H))) != FSA_OK) return rc;
+    if ((rc = grow(&P->d_htickets, &P->cap_htickets, 2 * static_cast<int64_t>(H))) != FSA_OK) return rc;
     if (P->cap_tickets != had || P->cap_htickets != had_h) P->tickets_fresh = true;
     if ((rc = grow(&P->d_mu, &P->cap_mu, static_cast<int64_t>(H) * D)) != FSA_OK) return rc;
     return grow(&P->d_elig, &P->cap_elig, static_cast<int64_t>(H));

@@ -90,7 +90,7 @@ struct NormsLaunch {
     uint8_t* eligible;     // [H]
     int center;            // 1: key norms about the head's mean key, c <q, mu> added to the bound
     float* mu;             // [H][D] workspace (center only)
-    unsigned* htickets;    // [H] workspace, zero between launches (center only)
+    unsigned* htickets;    // [2H] workspace, zero between launches: head key means (center), eligibility
     cudaStream_t stream;
 };
 

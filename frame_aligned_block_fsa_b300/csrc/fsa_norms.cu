@@ -13,8 +13,12 @@
 //                        the chunks in a fixed order into the frame's max key norm and key
 //                        sums (a ticket counter, no waiting);
 //   2. query_bounds      per (row chunk, frame, head): ||q||, bound = c ||q|| Kmax_S, and the
-//                        gap bound c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head;
-//   3. eligibility       per head: max gap bound <= tau.
+//                        gap bound c (||q|| Kmax_S - <q, kbar_S>), max-reduced per head; the
+//                        last block of a head to finish (a ticket counter) sets its
+//                        eligibility: max gap bound <= tau.
+// The query pass is a programmatic dependent launch: its blocks start while the key pass's last
+// blocks run, issue their first query loads, and wait for the key pass (griddepcontrol.wait)
+// only before they read its statistics.
 // With mean-centred keys (same section: keys share a large common component; subtracting
 // their mean tightens the bound and the softmax does not see it) the last frame of a head to
 // finish also forms the head's key mean mu from the frame sums, a second pass over K
@@ -59,6 +63,12 @@ __device__ __forceinline__ float group_sum(float v)
 }
 
 constexpr int kNormThreads = 256;
+
+// Programmatic dependent launch: a kernel lets the next one in the stream start (its blocks
+// may become resident once every block of this one has run this), and the next one waits for
+// this one to complete, with its writes visible, before it reads them.
+__device__ __forceinline__ void pdl_allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait_prerequisite() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 constexpr int kBatch = 2;  // row iterations whose loads are issued together (2 x 2 x 16 B per thread)
 
 // A thread reads 16 bf16 of a row as two 16-byte loads, D/2 columns apart, so that the row's
@@ -119,6 +129,7 @@ __global__ void __launch_bounds__(kNormThreads) key_frame_stats_kernel(
     __shared__ float wmax[kNormThreads / 32];
     __shared__ bool last;
     const int c = blockIdx.x, g = blockIdx.y, h = blockIdx.z;
+    pdl_allow_dependents();
     const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
     const int r0 = c * rows_per_chunk;
     const int r1 = min(T, r0 + rows_per_chunk);
@@ -225,6 +236,7 @@ __global__ void __launch_bounds__(kNormThreads) key_centred_max_kernel(
     constexpr int RPI = kNormThreads / TPR;
     __shared__ float wmax[kNormThreads / 32];
     const int c = blockIdx.x, g = blockIdx.y, h = blockIdx.z;
+    pdl_allow_dependents();
     const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
     const int r0 = c * rows_per_chunk;
     const int r1 = min(T, r0 + rows_per_chunk);
@@ -274,13 +286,15 @@ template <int D, bool CENTER>
 __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
     const uint16_t* __restrict__ q, int N, int T, int F, const int32_t* __restrict__ runs, float scale,
     const float* __restrict__ kmax, const float* __restrict__ ksum, const float* __restrict__ mu,
-    float* __restrict__ qnorm, float* __restrict__ bound, unsigned* __restrict__ gmax, int rows_per_block)
+    float* __restrict__ qnorm, float* __restrict__ bound, unsigned* __restrict__ gmax, int rows_per_block,
+    float tau, uint8_t* __restrict__ eligible, unsigned* __restrict__ etickets, int blocks_per_head)
 {
     constexpr int TPR = D / 16;
     constexpr int RPI = kNormThreads / TPR;
     __shared__ float kbar[D];
     __shared__ float kh_s;
     __shared__ float wmax[kNormThreads / 32];
+    __shared__ bool last;
     const int f = blockIdx.y, h = blockIdx.z;
     const int sub = threadIdx.x % TPR, rsel = threadIdx.x / TPR;
     const int r0 = blockIdx.x * rows_per_block;
@@ -295,6 +309,8 @@ __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
         const int r = r0 + b * RPI + rsel;
         load_row16<D>(base + static_cast<int64_t>(r) * (D / 8), sub, r < r1, ua[b], ub[b]);
     }
+    // the key statistics (and the zeroed gap maximum) come from the key pass
+    pdl_wait_prerequisite();
     const int32_t* rr = runs + f * kRunStride;
     const int n_runs = rr[0];
     if (threadIdx.x < D) {
@@ -372,6 +388,15 @@ __global__ void __launch_bounds__(kNormThreads) query_bounds_kernel(
         for (int w = 1; w < kNormThreads / 32; ++w) m = fmaxf(m, wmax[w]);
         // non-negative floats order like their bit patterns
         atomicMax(gmax + h, __float_as_uint(fmaxf(m, 0.0f)));
+        // the last block of this head to finish sets the head's eligibility
+        __threadfence();
+        last = atomicAdd(etickets + h, 1u) == static_cast<unsigned>(blocks_per_head - 1);
+    }
+    __syncthreads();
+    if (last && threadIdx.x == 0) {
+        __threadfence();
+        eligible[h] = static_cast<uint8_t>(__uint_as_float(__ldcg(gmax + h)) <= tau);
+        etickets[h] = 0u;  // ready for the next launch
     }
 }
 
@@ -402,14 +427,30 @@ static int launch_norms_d(const NormsLaunch& L)
     // about 256 query rows per block, split evenly over a frame (T = 1200: 5 blocks of 240)
     const int qblocks = (L.T + 255) / 256;
     const int rows_per_block = (L.T + qblocks - 1) / qblocks;
-    const dim3 grid(qblocks, L.F, L.H);
-    if (L.center)
-        query_bounds_kernel<D, true><<<grid, kNormThreads, 0, L.stream>>>(
-            L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum, L.mu, L.qnorm, L.bound, L.gmax, rows_per_block);
-    else
-        query_bounds_kernel<D, false><<<grid, kNormThreads, 0, L.stream>>>(
-            L.q, L.N, L.T, L.F, L.runs, L.scale, L.kmax, L.ksum, nullptr, L.qnorm, L.bound, L.gmax, rows_per_block);
-    eligibility_kernel<<<(L.H + 127) / 128, 128, 0, L.stream>>>(L.gmax, L.tau, L.eligible, L.H);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(qblocks, L.F, L.H);
+    cfg.blockDim = dim3(kNormThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = L.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    unsigned* etickets = L.htickets + L.H;
+    const cudaError_t e =
+        L.center ? cudaLaunchKernelEx(&cfg, query_bounds_kernel<D, true>, L.q, L.N, L.T, L.F, L.runs, L.scale,
+                                      static_cast<const float*>(L.kmax), static_cast<const float*>(L.ksum),
+                                      static_cast<const float*>(L.mu), L.qnorm, L.bound, L.gmax, rows_per_block,
+                                      L.tau, L.eligible, etickets, qblocks * L.F)
+                 : cudaLaunchKernelEx(&cfg, query_bounds_kernel<D, false>, L.q, L.N, L.T, L.F, L.runs, L.scale,
+                                      static_cast<const float*>(L.kmax), static_cast<const float*>(L.ksum),
+                                      static_cast<const float*>(nullptr), L.qnorm, L.bound, L.gmax, rows_per_block,
+                                      L.tau, L.eligible, etickets, qblocks * L.F);
+    if (e != cudaSuccess) {
+        note_cuda_error(e);
+        return -3;
+    }
     return launch_status();
 }
 

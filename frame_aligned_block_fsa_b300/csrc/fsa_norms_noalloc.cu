@@ -107,12 +107,12 @@ extern "C" int fsa_norms_noalloc(const uint16_t* q, const uint16_t* k, int H, in
     if (!q || !k || !kmax || !bound || !eligible) return FSA_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k)) & 15u) return FSA_ERR_INVALID_ARG;
 
-    // scratch layout: per-frame and per-head tickets | key runs of every query frame | per-frame
-    // key sums | per-chunk key sums | per-chunk max key norms | per-head gap maxima | per-head
-    // key means (used with centred keys)
+    // scratch layout: per-frame tickets and two per-head tickets | key runs of every query
+    // frame | per-frame key sums | per-chunk key sums | per-chunk max key norms | per-head gap
+    // maxima | per-head key means (used with centred keys)
     const size_t hf = static_cast<size_t>(H) * pv.F;
     const size_t chunks = static_cast<size_t>(fsa::norms_key_chunks(pv.T));
-    const size_t tickets_bytes = (hf + static_cast<size_t>(H)) * sizeof(unsigned);
+    const size_t tickets_bytes = (hf + 2 * static_cast<size_t>(H)) * sizeof(unsigned);
     const size_t runs_bytes = static_cast<size_t>(pv.F) * fsa::kRunStride * sizeof(int32_t);
     const size_t off_runs = fsa::round256(tickets_bytes);
     const size_t off_ksum = off_runs + fsa::round256(runs_bytes);

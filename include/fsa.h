@@ -278,7 +278,7 @@ int fsa_prep(const uint16_t* x, const uint16_t* w, int d_model, int H, int D, fs
  * host buffer is read on the stream.
  *   Arguments and results are those of fsa_norms, except that kmax, bound and eligible are
  *   required (they are the outputs; qnorm may be NULL).
- *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, (H*F + H)*4 + F*5*4 + H*F*D*4 +
+ *   Limit: with C = min(8, max(1, T/256)) key chunks per frame, (H*F + 2*H)*4 + F*5*4 + H*F*D*4 +
  *   H*F*C*D*4 + H*F*C*4 + H*4 + H*D*4 bytes (each part rounded up to 256) must fit in 2 MiB, e.g.
  *   H=24, F=24, T=1200, D=128 uses 1.4 MiB; larger problems return FSA_ERR_SCRATCH_LIMIT
  *   before any device work.
