@@ -11,29 +11,30 @@
 //    before it; heads that fail the eligibility test take the running-max path inside the
 //    same kernel.
 //
-// B300 design: a persistent kernel, one CTA per SM, 16 warps.  The work list is every
+// B300 design: a persistent kernel, one CTA per SM, 12 warps.  The work list is every
 // (head, frame, 128-row query tile); CTA b takes items b, b + G, b + 2G, ... (G CTAs), in
 // head-major, frame-major order, so the CTAs that run at the same time share their heads'
 // K and V in L2.  Every role walks the same item sequence and, per item, the frame's key runs
 // in key tiles of at most NK (<= 128) keys (the last tile of a run may be narrower, a multiple
 // of 16).  A tile counter g runs over all items of the CTA.
 //
-//   warps 0-11  softmax and epilogue, in three groups of four (warps 0-3, 4-7, 8-11), one warp
-//               per TMEM lane quarter: a thread owns one query row.  Every group takes every
-//               tile, its 16-key chunks c = group, group + 3, group + 6, so the twelve warps
-//               turn one tile into P together.  On norm-bound items each thread keeps a part of
-//               its row sum; on running-max items the groups also exchange their tile maxima
-//               through shared memory.
-//   warp 12     issues the S side (the warp runs the loop, one elected lane issues):
+//   warps 0-7   softmax and epilogue, in two groups of four (warps 0-3, 4-7), one warp per TMEM
+//               lane quarter: a thread owns one query row.  Every group takes every tile, its
+//               16-key chunks c = group + 2j (j = 0..3), so the eight warps turn one tile into P
+//               together, with equal shares.  On norm-bound items each thread keeps a part of its
+//               row sum; on running-max items the groups also exchange their tile maxima through
+//               shared memory.  (Two groups rather than three leave each SM sub-partition two
+//               busy softmax warps beside its control warp, and 168 registers a thread.)
+//   warp 8      issues the S side (the warp runs the loop, one elected lane issues):
 //                 Q(item)  -> TMEM by tcgen05.cp from shared memory (two Q slots, so the copy
 //                             for the next item never touches the one in use)
 //                 S(g)     = Q K(g)^T      A = Q from TMEM, B = K tile from shared memory
-//   warp 13     issues the PV side:
+//   warp 9      issues the PV side:
 //                 O       += P(g) V(g)     A = P from TMEM, B = V tile from shared memory
 //               (the pipe takes an MMA only when it has room, so an issuing thread is held for
 //               about as long as its MMAs run; with two issuers one does its bookkeeping while
 //               the other feeds the pipe)
-//   warps 14-15 TMA producers, one for Q and K, one for V: K(g) and V(g) go to slot g & 1 of a K
+//   warps 10-11 TMA producers, one for Q and K, one for V: K(g) and V(g) go to slot g & 1 of a K
 //               and a V ring (the slots of S buffer g & 1), each item's Q tile into its own
 //               staging buffer.
 //
@@ -44,7 +45,7 @@
 // one, against the same per-tile bookkeeping of the issuers (measured: 128-key tiles are the
 // fastest in both modes).
 //
-// One O accumulator: the epilogue of item k (O / l -> out) runs in all twelve softmax warps
+// One O accumulator: the epilogue of item k (O / l -> out) runs in all eight softmax warps
 // when the tile walk reaches item k + 1 (after they produced the P of its first tile), while
 // the pipe computes S of item k + 1; the first PV of item k + 1 waits until the epilogue has
 // read O out of TMEM.
@@ -63,18 +64,18 @@
 
 namespace fsa {
 
-constexpr int kGroups = 3;                  // softmax warp groups (tiles round-robin)
+constexpr int kGroups = 2;                  // softmax warp groups
 constexpr int kGroupWarps = 4;              // one warp per lane quarter
-constexpr int kSoftWarps = kGroups * kGroupWarps;  // 12
+constexpr int kSoftWarps = kGroups * kGroupWarps;  // 8
 constexpr int kAttnThreads = 32 * (kSoftWarps + 4);  // + two tcgen05 issuers and two TMA warps
 constexpr int kWarpS = kSoftWarps, kWarpPV = kSoftWarps + 1, kWarpTmaK = kSoftWarps + 2, kWarpTmaV = kSoftWarps + 3;
 constexpr int kNBuf = 2;                    // S buffers
 constexpr int kBufShift = 1;                // log2(kNBuf): tile g uses buffer g & (kNBuf - 1), phase g >> kBufShift
 constexpr int kBufCols = 128;               // TMEM columns (= keys) of an S buffer
-// The softmax turns a tile into P in two passes: chunks group and group + 3 of every group (the
-// first kPassChunks 16-key chunks), then chunk group + 6; the PV MMAs of the first pass's keys
-// start while the second pass runs.
-constexpr int kPassChunks = 2 * 3;
+// Group g takes the 16-key chunks c = g + 2j (j = 0..3) of every tile.  It hands P over in two
+// steps: after its chunks j = 0, 1 (over both groups: the first kPassChunks chunks), then after
+// j = 2, 3; the PV MMAs of the first step's keys start while the second step runs.
+constexpr int kPassChunks = 4;
 // Frames whose key runs are copied to shared memory when the kernel starts; larger plans
 // read them from global memory.
 constexpr int kSmemRunFrames = 256;
@@ -99,10 +100,10 @@ struct AttnCfg {
     static constexpr int B_QFULL = 2 * kNBuf;          // the staged Q tile landed
     static constexpr int B_QEMPTY = B_QFULL + 1;       // its copy into TMEM is done
     static constexpr int B_SFULL = B_QEMPTY + 1;       // kNBuf: S in buffer b complete (K slot b free)
-    // kNBuf: P of chunks 0-5 in buffer b written (the softmax's first pass: chunks group and
-    // group + 3 of every group): kSoftWarps arrivals, one from every softmax warp
+    // kNBuf: P of chunks 0-3 in buffer b written (the softmax's first step: chunks group and
+    // group + 2 of both groups): kSoftWarps arrivals, one from every softmax warp
     static constexpr int B_PFULL = B_SFULL + kNBuf;
-    // kNBuf: P of chunks 6-7 written (the second pass: chunk group + 6), kSoftWarps arrivals
+    // kNBuf: P of chunks 4-7 written (the second step), kSoftWarps arrivals
     static constexpr int B_PFULL2 = B_PFULL + kNBuf;
     static constexpr int B_OFULL = B_PFULL2 + kNBuf;   // the last PV of an item done: O final
     static constexpr int B_OFREE = B_OFULL + 1;        // the epilogue has read O (all softmax warps)
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                b0 + static_cast<uint64_t>((ks * 16 * 128) >> 4), C::IDESC_O, 1u);
             }
             __syncwarp();
-            // the last two chunks of P come from the softmax's second pass (every tile's phase of
+            // the last four chunks of P come from the softmax's second step (every tile's phase of
             // that barrier is waited for, so this thread never falls two phases behind)
             if (!(ok = __all_sync(0xffffffffu,
                                   wt.bar(p, bar(C::B_PFULL2 + buf), (g >> kBufShift) & 1, SITE_MMA_P))))
@@ -679,9 +680,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             l = 0.0f;
             if (p.stats && p.mode == 0 && !use_bound && warp == 0 && lane == 0 && loc == 0)
                 atomicAdd(&p.stats->fallback_heads, 1);
-            // Every group takes every tile: its 16-key chunks c = group, group + 3, group + 6 (the
-            // split of the row sum over the groups, and so its rounding, depends on the tile
-            // alone).  One loop per kind of item, so each stays small.
+            // Every group takes every tile: its 16-key chunks c = group + 2j (the split of the row
+            // sum over the groups, and so its rounding, depends on the tile alone).  One loop per kind of item, so each stays small.
             if (use_bound) {
                 const float nb2 = -b_nat * kLog2e;
                 for (int t = 0; t < n; ++t) {
@@ -698,17 +698,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after();
                     // p = 2^(s c2 - b log2 e) with the fixed bound, packed to bf16 over the first 8
                     // columns of each chunk just read; four partial sums of the fp32 weights.  Two
-                    // passes (chunks group and group + 3, then group + 6) bound the live scores.
+                    // steps of two chunks (group, group + 2; then group + 4, group + 6), each ending in
+                    // a hand-over of its P.
                     const float2 c2x2 = make_float2(c2, c2), nb2x2 = make_float2(nb2, nb2);
                     float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
 #pragma unroll 1
                     for (int ph = 0; ph < 2; ++ph) {
-                        const int c0 = group + 6 * ph;  // first chunk of this pass
-                        const bool u0 = c0 < nch, u1 = ph == 0 && c0 + 3 < nch;
+                        const int c0 = group + 4 * ph;  // first chunk of this step
+                        const bool u0 = c0 < nch, u1 = c0 + 2 < nch;
                         if (u0) {
                             float s[32];
                             tmem_ld_x16(tS + 16 * c0, s);
-                            if (u1) tmem_ld_x16(tS + 16 * (c0 + 3), s + 16);
+                            if (u1) tmem_ld_x16(tS + 16 * (c0 + 2), s + 16);
                             tmem_ld_wait();
 #pragma unroll
                             for (int i = 0; i < 32; ++i) reg_fence(s[i]);
@@ -730,11 +731,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                         a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
                                         a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
                                     }
-                                    tmem_st_x8(tS + 16 * (c0 + 3 * j), pk);
+                                    tmem_st_x8(tS + 16 * (c0 + 2 * j), pk);
                                 }
                             }
                         }
-                        // this pass's P is in TMEM: the PV MMAs of its chunks may start
+                        // this step's P is in TMEM: the PV MMAs of its chunks may start
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
@@ -764,22 +765,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // the exponentials use a reference m2 that moves only when the row max passes
                     // it by more than 8 (so every p stays below 2^8), and only then is the row's
                     // accumulator rescaled.
-                    const bool h0 = group < nch, h1 = group + 3 < nch, h2 = group + 6 < nch;
-                    float s[48];
+                    const bool h0 = group < nch, h1 = group + 2 < nch, h2 = group + 4 < nch, h3 = group + 6 < nch;
+                    float s[64];
                     if (h0) tmem_ld_x16(tS + 16 * group, s);
-                    if (h1) tmem_ld_x16(tS + 16 * (group + 3), s + 16);
-                    if (h2) tmem_ld_x16(tS + 16 * (group + 6), s + 32);
+                    if (h1) tmem_ld_x16(tS + 16 * (group + 2), s + 16);
+                    if (h2) tmem_ld_x16(tS + 16 * (group + 4), s + 32);
+                    if (h3) tmem_ld_x16(tS + 16 * (group + 6), s + 48);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int i = 0; i < 48; ++i) reg_fence(s[i]);
+                    for (int i = 0; i < 64; ++i) reg_fence(s[i]);
                     if constexpr (MASKED) {
                         // mask predicates, on tiles that are not wholly inside the row's interval
                         const int j0 = kst + t * p.NK;
                         if (!(j0 >= ja && j0 + width <= jb)) {
                             const unsigned span = static_cast<unsigned>(jb - ja);
 #pragma unroll
-                            for (int j = 0; j < 3; ++j) {
-                                const int cj = j0 + 16 * (group + 3 * j) - ja;
+                            for (int j = 0; j < 4; ++j) {
+                                const int cj = j0 + 16 * (group + 2 * j) - ja;
 #pragma unroll
                                 for (int e = 0; e < 16; ++e)
                                     if (static_cast<unsigned>(cj + e) >= span) s[16 * j + e] = -INFINITY;
@@ -788,8 +790,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     }
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) {
-                        if (j == 0 ? h0 : (j == 1 ? h1 : h2)) {
+                    for (int j = 0; j < 4; ++j) {
+                        if (j == 0 ? h0 : (j == 1 ? h1 : (j == 2 ? h2 : h3))) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) m4[e & 3] = fmaxf(m4[e & 3], s[16 * j + e]);
                         }
@@ -844,8 +846,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const float2 c2x2 = make_float2(c2, c2), nb2x2 = make_float2(nb2, nb2);
                     float2 a01 = make_float2(0.0f, 0.0f);  // two partial sums in one packed add
 #pragma unroll
-                    for (int j = 0; j < 3; ++j) {
-                        if (j == 0 ? h0 : (j == 1 ? h1 : h2)) {
+                    for (int j = 0; j < 4; ++j) {
+                        if (j == 0 ? h0 : (j == 1 ? h1 : (j == 2 ? h2 : h3))) {
                             float* sj = s + 16 * j;
                             uint32_t pk[8];
 #pragma unroll
@@ -858,10 +860,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
 #pragma unroll
                             for (int i = 0; i < 16; i += 2) a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
-                            tmem_st_x8(tS + 16 * (group + 3 * j), pk);
+                            tmem_st_x8(tS + 16 * (group + 2 * j), pk);
                         }
                         if (j == 1) {
-                            // chunks group and group + 3 are in TMEM: the first pass is done
+                            // chunks group and group + 2 are in TMEM: the first step is done
                             tmem_st_wait();
                             tc_fence_before();
                             __syncwarp();
