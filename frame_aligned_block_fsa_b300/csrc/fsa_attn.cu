@@ -600,10 +600,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) reg_fence(o[i]);
                     if (rvalid) {
+                        // streaming stores: out is read by no one in this kernel, and lines that linger
+                        // in L2 would displace the K and V tiles the CTAs re-read
 #pragma unroll
                         for (int e = 0; e < 4; ++e)
-                            dst[4 * c + e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l, o[4 * e + 2] * inv_l,
-                                                         o[4 * e + 3] * inv_l);
+                            __stcs(dst + 4 * c + e, make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l,
+                                                                o[4 * e + 2] * inv_l, o[4 * e + 3] * inv_l));
                     }
                 }
             }
