@@ -9,7 +9,8 @@
 //    the per-row upper bound b_i = c ||q_i|| max ||k_j|| computed beforehand, so
 //    p = exp(s - b_i) needs no rescale of the accumulator, and no tile depends on the one
 //    before it; heads that fail the eligibility test take the running-max path inside the
-//    same kernel.
+//    same kernel.  Launches that run the running-max path alone use an instantiation without
+//    the norm-bound loop (BOUND = false), so that loop does not shape its register allocation.
 //
 // B300 design: a persistent kernel, one CTA per SM, 12 warps.  The work list is every
 // (head, frame, 128-row query tile); CTA b takes items b, b + G, b + 2G, ... (G CTAs), in
@@ -24,7 +25,10 @@
 //               together, with equal shares.  On norm-bound items each thread keeps a part of its
 //               row sum; on running-max items the groups also exchange their tile maxima through
 //               shared memory.  (Two groups rather than three leave each SM sub-partition two
-//               busy softmax warps beside its control warp, and 168 registers a thread.)
+//               busy softmax warps beside its control warp, and up to 168 registers a thread.)
+//               Norm-bound items read a tile's scores in two sets of 16 columns: the load of a
+//               set's next chunk goes out as soon as the set is packed, so its TMEM latency
+//               hides behind the other set's arithmetic.
 //   warp 8      issues the S side (the warp runs the loop, one elected lane issues):
 //                 Q(item)  -> TMEM by tcgen05.cp from shared memory (two Q slots, so the copy
 //                             for the next item never touches the one in use)
@@ -270,7 +274,7 @@ struct AttnWait {
     }
 };
 
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool BOUND>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     fsa_attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                         const __grid_constant__ CUtensorMap tmV, const AttnParams p)
@@ -672,7 +676,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 row0 = f * p.T + qt * 128;
             }
             const int n = n0 + n1;
-            const bool use_bound = !MASKED && p.mode == 0 && p.bound != nullptr && nx_el != 0;
+            const bool use_bound = BOUND && !MASKED && p.mode == 0 && p.bound != nullptr && nx_el != 0;
             flags = valid | (use_bound ? 1 << 8 : 0);
             grow = h * p.N + row0 + row;
             b_nat = nx_b;
@@ -704,45 +708,50 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     // a hand-over of its P.
                     const float2 c2x2 = make_float2(c2, c2), nb2x2 = make_float2(nb2, nb2);
                     float2 a01 = make_float2(0.0f, 0.0f), a23 = make_float2(0.0f, 0.0f);
-#pragma unroll 1
-                    for (int ph = 0; ph < 2; ++ph) {
-                        const int c0 = group + 4 * ph;  // first chunk of this step
-                        const bool u0 = c0 < nch, u1 = c0 + 2 < nch;
-                        if (u0) {
-                            float s[32];
-                            tmem_ld_x16(tS + 16 * c0, s);
-                            if (u1) tmem_ld_x16(tS + 16 * (c0 + 2), s + 16);
-                            tmem_ld_wait();
+                    const bool h0 = group < nch, h1 = group + 2 < nch, h2 = group + 4 < nch,
+                               h3 = group + 6 < nch;
+                    auto chunk = [&](float* sj, int c) {
+                        uint32_t pk[8];
 #pragma unroll
-                            for (int i = 0; i < 32; ++i) reg_fence(s[i]);
-#pragma unroll
-                            for (int j = 0; j < 2; ++j) {
-                                if (j == 0 || u1) {
-                                    float* sj = s + 16 * j;
-                                    uint32_t pk[8];
-#pragma unroll
-                                    for (int i = 0; i < 16; i += 2) {
-                                        const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
-                                        sj[i] = ex2(e.x);
-                                        sj[i + 1] = ex2(e.y);
-                                    }
-#pragma unroll
-                                    for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
-#pragma unroll
-                                    for (int i = 0; i < 16; i += 4) {
-                                        a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
-                                        a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
-                                    }
-                                    tmem_st_x8(tS + 16 * (c0 + 2 * j), pk);
-                                }
-                            }
+                        for (int i = 0; i < 16; i += 2) {
+                            const float2 e = __ffma2_rn(make_float2(sj[i], sj[i + 1]), c2x2, nb2x2);
+                            sj[i] = ex2(e.x);
+                            sj[i + 1] = ex2(e.y);
                         }
-                        // this step's P is in TMEM: the PV MMAs of its chunks may start
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(sj[2 * i], sj[2 * i + 1]);
+#pragma unroll
+                        for (int i = 0; i < 16; i += 4) {
+                            a01 = __fadd2_rn(a01, make_float2(sj[i], sj[i + 1]));
+                            a23 = __fadd2_rn(a23, make_float2(sj[i + 2], sj[i + 3]));
+                        }
+                        tmem_st_x8(tS + 16 * c, pk);
+                    };
+                    auto hand_over = [&](int b_full) {
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(bar((ph == 0 ? C::B_PFULL : C::B_PFULL2) + buf));
-                    }
+                        if (lane == 0) mbar_arrive(bar(b_full + buf));
+                    };
+                    // two 16-column register sets: the next chunk's load goes out as soon as
+                    // its set is free, so its latency hides behind the other set's arithmetic
+                    float r0[16], r1[16];
+                    if (h0) tmem_ld_x16(tS + 16 * group, r0);
+                    if (h1) tmem_ld_x16(tS + 16 * (group + 2), r1);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) { reg_fence(r0[i]); reg_fence(r1[i]); }
+                    if (h0) chunk(r0, group);
+                    if (h2) tmem_ld_x16(tS + 16 * (group + 4), r0);
+                    if (h1) chunk(r1, group + 2);
+                    if (h3) tmem_ld_x16(tS + 16 * (group + 6), r1);
+                    hand_over(C::B_PFULL);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) { reg_fence(r0[i]); reg_fence(r1[i]); }
+                    if (h2) chunk(r0, group + 4);
+                    if (h3) chunk(r1, group + 6);
+                    hand_over(C::B_PFULL2);
                     l += (a01.x + a01.y) + (a23.x + a23.y);
                     if (pv_flags >= 0) {
                         if (!(ok = epilogue())) break;
@@ -925,11 +934,11 @@ __global__ void fsa_selftest_wait_kernel(long long limit, int* status)
     }
 }
 
-template <int D, bool MASKED>
+template <int D, bool MASKED, bool BOUND>
 static int launch_attn(const AttnLaunch& L)
 {
     using C = AttnCfg<D>;
-    auto kern = fsa_attn_fwd_kernel<D, MASKED>;
+    auto kern = fsa_attn_fwd_kernel<D, MASKED, BOUND>;
     static bool attr_done = false;  // per instantiation
     if (!attr_done) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -957,8 +966,13 @@ int launch_attention(const AttnLaunch& L)
     static_assert(kMaxKeyTile == kBufCols, "one key tile fills an S buffer at most");
     if (L.params.NK < 16 || L.params.NK > kMaxKeyTile || L.params.NK % 16 != 0) return -2;
     if (L.masked && (L.params.mode != 1 || L.params.bound != nullptr || L.params.NK != kMaxKeyTile)) return -2;
-    if (L.D == 64) return L.masked ? launch_attn<64, true>(L) : launch_attn<64, false>(L);
-    if (L.D == 128) return L.masked ? launch_attn<128, true>(L) : launch_attn<128, false>(L);
+    const bool bound = !L.masked && L.params.mode == 0;
+    if (L.D == 64)
+        return L.masked ? launch_attn<64, true, false>(L)
+                        : (bound ? launch_attn<64, false, true>(L) : launch_attn<64, false, false>(L));
+    if (L.D == 128)
+        return L.masked ? launch_attn<128, true, false>(L)
+                        : (bound ? launch_attn<128, false, true>(L) : launch_attn<128, false, false>(L));
     return -2;
 }
 
