@@ -127,7 +127,12 @@ struct AttnCfg {
     static constexpr int MMAX_OFF = LSUM_OFF + LSUM_BYTES;
     static constexpr int MMAX_BYTES = 2 * kGroups * 128 * 4;
     static constexpr int RUNS_OFF = MMAX_OFF + MMAX_BYTES;
-    static constexpr int SMEM_USED = RUNS_OFF + kSmemRunFrames * kRunStride * 4;
+    // per softmax warp: 32 rows x 32 columns of out (fp32), rows 144 B apart so that both the
+    // row-per-lane writes and the 8-lanes-per-row reads are free of bank conflicts
+    static constexpr int OSTG_ROW = 32 * 4 + 16;
+    static constexpr int OSTG_WARP = 32 * OSTG_ROW;
+    static constexpr int OSTG_OFF = (RUNS_OFF + kSmemRunFrames * kRunStride * 4 + 15) & ~15;
+    static constexpr int SMEM_USED = OSTG_OFF + kSoftWarps * OSTG_WARP;
     // room to align the buffers to 1024 B, and at least half of the SM's shared memory, so two
     // CTAs never share an SM (each takes all 512 TMEM columns)
     static constexpr int SMEM_BYTES = SMEM_USED + 1024 > 120 * 1024 ? SMEM_USED + 1024 : 120 * 1024;
@@ -572,8 +577,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // over the groups (each summed its own tiles); they exchange the parts first, and add
         // them in group order.  False on abort.
         auto epilogue = [&]() -> bool {
-            constexpr int NCH = D / 16;
-            const int cb = group * NCH / kGroups, ce = (group + 1) * NCH / kGroups;
             const int item = pv_flags >> 9;
             const uint32_t ls_count = sbase + C::MISC_OFF + 8u + 4u * quarter;
             const uint32_t ls = sbase + C::LSUM_OFF + (item & 1) * (kGroups * 128 * 4) + 4u * row;
@@ -593,30 +596,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!__all_sync(0xffffffffu, wt.bar(p, bar(C::B_OFULL), item & 1, SITE_SOFT_O))) return false;
             tc_fence_after();
             const uint32_t tO = tbase + lane_off + C::T_O;
-            float4* dst = reinterpret_cast<float4*>(p.out + static_cast<int64_t>(pv_grow) * D);
+            // The group's D/2 columns in parts of 32: read from TMEM (this lane's row), scaled
+            // into the warp's staging rows, then written with 8 lanes per row, so that each
+            // store covers four whole 128-byte lines instead of touching 32 rows.  O is released
+            // once its last part is in registers.
+            constexpr int PARTS = D / 64;
+            const int c0 = group * (D / 2);
+            const int valid_rows = pv_flags & 0xff;
+            float* out_w = p.out + static_cast<int64_t>(pv_grow - lane) * D + c0;  // the warp's row 0
+            float* stg = reinterpret_cast<float*>(sgen + C::OSTG_OFF + warp * C::OSTG_WARP);
 #pragma unroll
-            for (int j = 0; j < (NCH + kGroups - 1) / kGroups; ++j) {
-                const int c = cb + j;
-                if (c < ce) {
+            for (int part = 0; part < PARTS; ++part) {
+                float4* srow = reinterpret_cast<float4*>(stg + lane * (C::OSTG_ROW / 4));
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
                     float o[16];
-                    tmem_ld_x16(tO + 16 * c, o);
+                    tmem_ld_x16(tO + c0 + 32 * part + 16 * half, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) reg_fence(o[i]);
-                    if (rvalid) {
-                        // streaming stores: out is read by no one in this kernel, and lines that linger
-                        // in L2 would displace the K and V tiles the CTAs re-read
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            __stcs(dst + 4 * c + e, make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l,
-                                                                o[4 * e + 2] * inv_l, o[4 * e + 3] * inv_l));
+                    if (part == PARTS - 1 && half == 1) {
+                        // every read of O by this warp is complete: the next item may overwrite O
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(bar(C::B_OFREE));
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        srow[4 * half + e] = make_float4(o[4 * e] * inv_l, o[4 * e + 1] * inv_l,
+                                                         o[4 * e + 2] * inv_l, o[4 * e + 3] * inv_l);
                 }
+                __syncwarp();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int r = 4 * k + (lane >> 3);
+                    const float4 v = reinterpret_cast<const float4*>(stg + r * (C::OSTG_ROW / 4))[lane & 7];
+                    // streaming stores: out is read by no one in this kernel, and lines that
+                    // linger in L2 would displace the K and V tiles the CTAs re-read
+                    if (32 * quarter + r < valid_rows)
+                        __stcs(reinterpret_cast<float4*>(out_w + static_cast<int64_t>(r) * D + 32 * part) + (lane & 7), v);
+                }
+                __syncwarp();  // the staging rows are rewritten by the next part
             }
-            // every read of O by this warp is complete: the next item may overwrite O
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(C::B_OFREE));
             if (group == 0) {
                 const float m_nat = pv_mt * kLn2;
                 bool under = false;
